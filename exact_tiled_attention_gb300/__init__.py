@@ -1,0 +1,22 @@
+"""exact_tiled_attention_gb300 -- exact tiled attention for GB300 (sm_103a).
+
+The computation lives in libgbattn.so (hand-written CUDA: TMA + tcgen05 +
+TMEM prefill forward, split-KV decode with a merge kernel) behind the C ABI in
+include/gbattn.h.  This package is its Python binding; it loads the library on
+first use and raises if it is missing (there is no fallback path).
+"""
+from .binding import (  # noqa: F401
+    EXPORTS,
+    GbattnError,
+    LIB_PATH,
+    attn_decode_splitkv,
+    attn_decode_workspace_bytes,
+    attn_fwd,
+    error_string,
+    gbattn_causal_tile_counts,
+    gbattn_device_status,
+    gbattn_version,
+    load_library,
+)
+
+__version__ = "0.1.0"

@@ -1,0 +1,201 @@
+"""Thin Python binding of libgbattn.so (argument marshalling only).
+
+Every step of the attention computation runs in the CUDA kernels behind the
+C ABI declared in include/gbattn.h; this module only checks tensor metadata,
+allocates outputs through PyTorch (device memory and streams are PyTorch's)
+and forwards raw device pointers.  There is no CPU or PyTorch fallback: if the
+library is missing or the current device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbattn.so")
+
+GBATTN_OK = 0
+GBATTN_F16 = 0
+GBATTN_BF16 = 1
+ERRORS = {
+    -1: "GBATTN_EBADSHAPE", -2: "GBATTN_EHEADS", -3: "GBATTN_EHEADDIM", -4: "GBATTN_EDTYPE",
+    -5: "GBATTN_EPOINTER", -6: "GBATTN_EWORKSPACE", -7: "GBATTN_ELAUNCH",
+    -8: "GBATTN_EDEVICE_TIMEOUT", -9: "GBATTN_ESPLIT", -10: "GBATTN_EUNSUPPORTED",
+}
+EXPORTS = ("attn_fwd", "attn_decode_workspace_bytes", "attn_decode_splitkv",
+           "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_error_string",
+           "gbattn_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GbattnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({error_string(code)})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libgbattn.so (built by exact_tiled_attention_gb300._build).  Raises
+    if it is missing: there is no fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m exact_tiled_attention_gb300._build` (no fallback exists)")
+        lib = ctypes.CDLL(path)
+        vp, ci, cf, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        ll_p = ctypes.POINTER(ctypes.c_longlong)
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
+        lib.attn_fwd.restype = ci
+        lib.attn_decode_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.attn_decode_workspace_bytes.restype = sz
+        lib.attn_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, sz,
+                                            ci, vp]
+        lib.attn_decode_splitkv.restype = ci
+        lib.gbattn_causal_tile_counts.argtypes = [ci, ci, ci, ci, ll_p, ll_p, ll_p, ll_p, ll_p]
+        lib.gbattn_causal_tile_counts.restype = ci
+        lib.gbattn_device_status.argtypes = []
+        lib.gbattn_device_status.restype = ci
+        lib.gbattn_error_string.argtypes = [ci]
+        lib.gbattn_error_string.restype = ctypes.c_char_p
+        lib.gbattn_version.argtypes = []
+        lib.gbattn_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def error_string(code: int) -> str:
+    try:
+        return load_library().gbattn_error_string(int(code)).decode()
+    except Exception:  # library not loadable: still produce a message
+        return ERRORS.get(code, str(code))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return GBATTN_F16
+    if t.dtype == torch.bfloat16:
+        return GBATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float16 or bfloat16")
+
+
+def _check(t: torch.Tensor, name: str, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous ([B, heads, S, d] row-major)")
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None, lse=None,
+             return_lse: bool = True, stream=None):
+    """Exact attention forward through the C ABI `attn_fwd`.
+
+    q [B,H,Sq,d], k/v [B,Hkv,Sk,d] (fp16 or bf16, CUDA, contiguous).
+    Returns (o [B,H,Sq,d] in q's dtype, lse [B,H,Sq] fp32 or None)."""
+    _check(q, "q", 4)
+    _check(k, "k", 4)
+    _check(v, "v", 4)
+    B, H, Sq, d = q.shape
+    Bk, Hkv, Sk, dk = k.shape
+    if k.shape != v.shape or Bk != B or dk != d:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    rc = lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                      lse.data_ptr() if lse is not None else None, B, H, Hkv, Sq, Sk, d, float(scale),
+                      int(bool(causal)), dt, _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_decode_workspace_bytes(B: int, Hq: int, n_split: int, d: int) -> int:
+    return int(load_library().attn_decode_workspace_bytes(B, Hq, n_split, d))
+
+
+def attn_decode_splitkv(q, k_cache, v_cache, seqlens, scale: float | None = None, n_split: int = 16,
+                        workspace=None, out=None, lse=None, return_lse: bool = True, stream=None):
+    """One-query split-KV decode through the C ABI `attn_decode_splitkv`.
+
+    q [B,Hq,1,d]; k_cache/v_cache [B,Hkv,Sk_max,d]; seqlens [B] int32 (CUDA).
+    workspace: optional caller-owned fp32/uint8 CUDA buffer of at least
+    attn_decode_workspace_bytes(B, Hq, n_split, d) bytes (allocated here if
+    omitted).  Returns (o [B,Hq,1,d], lse [B,Hq] or None, workspace)."""
+    _check(q, "q", 4)
+    _check(k_cache, "k_cache", 4)
+    _check(v_cache, "v_cache", 4)
+    if not isinstance(seqlens, torch.Tensor) or not seqlens.is_cuda or seqlens.dtype != torch.int32:
+        raise ValueError("seqlens must be an int32 CUDA tensor")
+    B, Hq, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes exactly one query per sequence: q [B,Hq,1,d]")
+    Bk, Hkv, Sk_max, dk = k_cache.shape
+    if k_cache.shape != v_cache.shape or Bk != B or dk != d or seqlens.numel() != B:
+        raise ValueError("shape mismatch between q, caches and seqlens")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q and the caches must share one dtype")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lib = load_library()
+    need = int(lib.attn_decode_workspace_bytes(B, Hq, n_split, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    rc = lib.attn_decode_splitkv(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                 seqlens.data_ptr(), out.data_ptr(),
+                                 lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Sk_max, d,
+                                 float(scale), int(n_split), workspace.data_ptr(), ws_bytes, dt,
+                                 _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "attn_decode_splitkv")
+    return out, lse, workspace
+
+
+def gbattn_causal_tile_counts(Sq: int, Sk: int, Br: int, Bc: int) -> dict:
+    """Host planner: full / partial / skipped causal tiles and cell counts."""
+    vals = [ctypes.c_longlong() for _ in range(5)]
+    rc = load_library().gbattn_causal_tile_counts(Sq, Sk, Br, Bc, *[ctypes.byref(x) for x in vals])
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "gbattn_causal_tile_counts")
+    keys = ("full", "partial", "skipped", "allowed_cells", "visited_cells")
+    return {k: v.value for k, v in zip(keys, vals)}
+
+
+def gbattn_device_status() -> int:
+    """Synchronise and read/clear the kernels' status word (0 = ok)."""
+    return int(load_library().gbattn_device_status())
+
+
+def gbattn_version() -> str:
+    return load_library().gbattn_version().decode()

@@ -1,0 +1,258 @@
+// gbattn_api.cu -- the C ABI (include/gbattn.h): argument validation, host
+// planning helpers, tensor-map encoding and dispatch to the kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "../../include/gbattn.h"
+#include "gbattn_internal.h"
+
+namespace gbattn {
+
+// Device status word written by the kernels' bounded waits (0 = ok).
+__device__ int g_device_status;
+
+namespace {
+
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+// Device status pointer per device (looked up once, then cached).
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+int g_sm_major[kMaxDevices] = {};
+int g_sm_minor[kMaxDevices] = {};
+std::mutex g_dev_mutex;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Returns GBATTN_OK and the status pointer of the current device, or an error.
+int current_device(int** status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return GBATTN_EUNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return GBATTN_EUNSUPPORTED;
+    }
+    g_sm_major[dev] = major;
+    g_sm_minor[dev] = minor;
+    if (major != 10 || minor != 3) return GBATTN_EUNSUPPORTED;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) {
+      cudaGetLastError();
+      return GBATTN_ELAUNCH;
+    }
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  if (g_sm_major[dev] != 10 || g_sm_minor[dev] != 3) return GBATTN_EUNSUPPORTED;
+  *status = g_status_ptr[dev];
+  return GBATTN_OK;
+}
+
+}  // namespace
+
+EncodeTiledFn encode_tiled_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    else
+      cudaGetLastError();
+  });
+  return g_encode;
+}
+
+bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, int d, int rows, long long outer,
+                  int box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r =
+      enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace gbattn
+
+using namespace gbattn;
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Hkv, int Sq, int Sk, int d, float scale, int causal, int dtype, void* stream) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return GBATTN_EBADSHAPE;
+  if (H % Hkv != 0) return GBATTN_EHEADS;
+  if (d != 64 && d != 128) return GBATTN_EHEADDIM;
+  if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
+  if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return GBATTN_EPOINTER;
+  // Tensor-map extents are 32-bit per dimension except the outermost.
+  if (static_cast<long long>(B) * H > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
+    return GBATTN_EBADSHAPE;
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.bf16 = dtype == GBATTN_BF16;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status;
+  return launch_prefill(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
+size_t attn_decode_workspace_bytes(int B, int Hq, int n_split, int d) {
+  if (B < 1 || Hq < 1 || n_split < 1 || d < 1) return 0;
+  return static_cast<size_t>(B) * Hq * n_split * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+                        void* o, float* lse, int B, int Hq, int Hkv, int Sk_max, int d, float scale,
+                        int n_split, void* workspace, size_t workspace_bytes, int dtype,
+                        void* stream) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sk_max < 1) return GBATTN_EBADSHAPE;
+  if (B > 65535) return GBATTN_EBADSHAPE;
+  if (Hq % Hkv != 0) return GBATTN_EHEADS;
+  if (d != 64 && d != 128) return GBATTN_EHEADDIM;
+  if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
+  if (n_split < 1 || n_split > 256) return GBATTN_ESPLIT;
+  if (!q || !k_cache || !v_cache || !seqlens || !o || !workspace || !aligned16(q) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(seqlens) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return GBATTN_EPOINTER;
+  if (workspace_bytes < attn_decode_workspace_bytes(B, Hq, n_split, d)) return GBATTN_EWORKSPACE;
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  DecodeArgs a;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.seqlens = seqlens;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Sk_max = Sk_max;
+  a.d = d;
+  a.scale = scale;
+  a.n_split = n_split;
+  a.workspace = static_cast<float*>(workspace);
+  a.bf16 = dtype == GBATTN_BF16;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status;
+  return launch_decode(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
+int gbattn_causal_tile_counts(int Sq, int Sk, int Br, int Bc, long long* full, long long* partial,
+                              long long* skipped, long long* allowed_cells,
+                              long long* visited_cells) {
+  if (Sq < 1 || Sk < 1 || Br < 1 || Bc < 1) return GBATTN_EBADSHAPE;
+  const long long delta = static_cast<long long>(Sk) - Sq;
+  long long nf = 0, np = 0, ns = 0, allowed = 0, visited = 0;
+  const int tq = (Sq + Br - 1) / Br, tk = (Sk + Bc - 1) / Bc;
+  for (int i = 0; i < tq; ++i) {
+    const long long q0 = static_cast<long long>(i) * Br;
+    const long long q1 = q0 + Br < Sq ? q0 + Br : Sq;
+    for (int j = 0; j < tk; ++j) {
+      const long long k0 = static_cast<long long>(j) * Bc;
+      const long long k1 = k0 + Bc < Sk ? k0 + Bc : Sk;
+      if (k0 > (q1 - 1) + delta) {
+        ++ns;
+        continue;
+      }
+      if (k1 - 1 <= q0 + delta)
+        ++nf;
+      else
+        ++np;
+      visited += (q1 - q0) * (k1 - k0);
+    }
+  }
+  for (long long i = 0; i < Sq; ++i) {
+    long long last = i + delta;  // largest visible key of row i
+    if (last >= Sk) last = Sk - 1;
+    if (last >= 0) allowed += last + 1;
+  }
+  if (full) *full = nf;
+  if (partial) *partial = np;
+  if (skipped) *skipped = ns;
+  if (allowed_cells) *allowed_cells = allowed;
+  if (visited_cells) *visited_cells = visited;
+  return GBATTN_OK;
+}
+
+int gbattn_device_status(void) {
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return GBATTN_ELAUNCH;
+  }
+  int value = 0;
+  if (cudaMemcpyFromSymbol(&value, g_device_status, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return GBATTN_ELAUNCH;
+  }
+  if (value != 0) {
+    const int zero = 0;
+    cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int));
+    return GBATTN_EDEVICE_TIMEOUT;
+  }
+  return GBATTN_OK;
+}
+
+const char* gbattn_error_string(int code) {
+  switch (code) {
+    case GBATTN_OK: return "ok";
+    case GBATTN_EBADSHAPE: return "bad shape (a size is < 1 or too large)";
+    case GBATTN_EHEADS: return "query heads are not a multiple of KV heads";
+    case GBATTN_EHEADDIM: return "unsupported head dimension (only 64 and 128)";
+    case GBATTN_EDTYPE: return "unsupported dtype (only fp16 and bf16)";
+    case GBATTN_EPOINTER: return "null or misaligned pointer";
+    case GBATTN_EWORKSPACE: return "decode workspace too small";
+    case GBATTN_ELAUNCH: return "CUDA launch or tensor-map encoding failed";
+    case GBATTN_EDEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case GBATTN_ESPLIT: return "n_split out of range (1..256)";
+    case GBATTN_EUNSUPPORTED: return "no sm_103 device is current";
+    default: return "unknown status code";
+  }
+}
+
+const char* gbattn_version(void) { return "gbattn 0.1.0 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// gbattn_internal.h -- host-side declarations shared by the library's
+// translation units (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gbattn {
+
+// Arguments of one prefill launch (already validated by the C-ABI layer).
+struct PrefillArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, Hkv, Sq, Sk, d;
+  float scale;
+  int causal;
+  bool bf16;
+  cudaStream_t stream;
+  int* status;  // device status word
+};
+
+// Arguments of one split-KV decode (partial + merge) launch.
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const int* seqlens;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, Sk_max, d;
+  float scale;
+  int n_split;
+  float* workspace;
+  bool bf16;
+  cudaStream_t stream;
+  int* status;
+};
+
+// Each returns a cudaError_t / CUresult folded into 0 (ok) or -1 (launch or
+// tensor-map failure).
+int launch_prefill(const PrefillArgs& a);
+int launch_decode(const DecodeArgs& a);
+
+// cuTensorMapEncodeTiled fetched once through the runtime's driver entry
+// point (no link-time dependency on libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled_fn();
+
+// 3-D tensor map over a contiguous [outer, rows, d] 16-bit tensor with a
+// (64 x box_rows x 1) box and 128-byte swizzle; rows past `rows` read as 0.
+bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, int d, int rows, long long outer,
+                  int box_rows);
+
+}  // namespace gbattn

@@ -1,0 +1,486 @@
+// prefill_fwd.cu -- exact attention forward on sm_103a: TMA-fed shared-memory
+// ring, tcgen05 MMAs accumulating in tensor memory, warp-specialised roles.
+//
+// One CTA owns a pair of 128-row query tiles ("H" = rows [256p, 256p+128),
+// "L" = the next 128 rows) of one (batch, query head) and streams every
+// visible 128-key K/V tile of that head's KV head once for both query tiles
+// (M4.4 0x03 Algorithm 1: query-tile owner; M4.6 0x08: two query tiles per
+// CTA so one tile's softmax overlaps the other tile's tensor-core work).
+//
+// Tensor memory map (512 columns, 128 lanes; lane = query row of the tile):
+//   S_H  [  0,128)  fp32 scores of tile H;  P_H (16-bit) aliases [ 64,128)
+//   S_L  [128,256)  fp32 scores of tile L;  P_L (16-bit) aliases [192,256)
+//   O_H  [256,256+d)        unnormalised output accumulator of tile H
+//   O_L  [256+d,256+2d)     same for tile L
+// (M4.6 0x07 "Derive The Pinned Beta23 TMEM Map": 2N + 2 d_v <= 512.)
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax + correction + epilogue of tile H (thread = one row)
+//   warps 4-7  the same for tile L
+//   warp  8    TMEM allocation; lane 0 issues every tcgen05.mma and commit
+//   warp  9    lane 0 issues every TMA copy (Q once, then K_j, V_j)
+//
+// MMA issue order (M4.6 0x08 startup / steady / drain):
+//   QK_H(0) QK_L(0) | PV_H(j-1) QK_H(j) PV_L(j-1) QK_L(j) ... | PV_H PV_L
+// P_X(j-1) lives in the columns QK_X(j) overwrites; as in the pages' FA4
+// schedule, PV_X(j-1) is issued by the same thread before QK_X(j).
+//
+// Online softmax (M4.3 0x07-0x09; M4.6 0x09 conditional rescaling): each
+// softmax thread keeps its row's retained reference r (raw score units) and
+// denominator l in registers.  With lambda = scale*log2(e), a new tile with
+// row maximum mx gives candidate c = max(r, mx); the reference moves only if
+// (c - r)*lambda > 8, in which case l and the row of O are multiplied by
+// gamma = 2^((r - c)*lambda).  P = 2^(lambda*s - lambda*r) <= 2^8 is rounded
+// to the input dtype for the PV MMA while l accumulates the fp32 values.
+// Epilogue: O = O / l,  LSE = (lambda*r + log2 l) * ln 2.
+//
+// Causal (M4.4 0x05.1A-D, bottom-right delta = Sk - Sq): key tiles wholly in
+// the future are never loaded or multiplied; tiles crossing the diagonal or
+// the key tail are masked element-wise to -inf before the row maximum.
+#include <cuda_runtime.h>
+
+#include "gbattn_internal.h"
+#include "gbattn_ptx.cuh"
+
+namespace gbattn {
+namespace {
+
+constexpr int kBM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units (fp16/bf16 row of M4.6 0x09 table)
+
+template <int D>
+struct Cfg {
+  static constexpr int kColBlocks = D / 64;           // 128-byte swizzle column blocks
+  static constexpr int kTileBytes = kBM * D * 2;      // one 128 x D 16-bit tile
+  static constexpr int kBlockBytes = kBM * 128;       // one 128-row x 128-byte block
+  static constexpr int kStages = (D == 128) ? 4 : 6;  // K/V ring slots
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
+  static constexpr int kSmemBytes = 1024 + kBarOff + 512;  // + alignment slack + barriers
+};
+
+struct Params {
+  void* o;
+  float* lse;
+  int B, H, Hkv, Sq, Sk, g;
+  int n_pairs;
+  int delta;
+  float scale_log2;
+  int causal;
+  int* status;
+};
+
+struct __align__(8) Barriers {
+  uint64_t q_full;
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Number of key tiles query tile [q0, q0+128) visits (0 if the tile is empty
+// or every row is fully masked): M4.4 0x05.1D n_block_max with the
+// bottom-right offset.
+__device__ __forceinline__ int tiles_for(int q0, int Sq, int Sk, int causal, int delta) {
+  if (q0 >= Sq) return 0;
+  const int nk = ceil_div(Sk, kBN);
+  if (!causal) return nk;
+  const int last_row = min(q0 + kBM - 1, Sq - 1);
+  const int lim = last_row + delta;  // largest visible key of the tile
+  if (lim < 0) return 0;
+  return min(nk, lim / kBN + 1);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                       const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + C::kQOff;
+  uint8_t* sRing = smem + C::kRingOff;
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kBarOff);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- work unit: heaviest query pairs first (causal), heads fastest
+  const int BH = p.B * p.H;
+  const int bh = blockIdx.x % BH;
+  const int pair = p.n_pairs - 1 - blockIdx.x / BH;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int kvh = h / p.g;
+  int n_tiles[2];
+  int q0[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    q0[x] = pair * 2 * kBM + x * kBM;
+    n_tiles[x] = tiles_for(q0[x], p.Sq, p.Sk, CAUSAL ? 1 : 0, p.delta);
+  }
+  const int n_max = max(n_tiles[0], n_tiles[1]);
+
+  // ---- setup
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->p_full[x], kBM);
+      mbar_init(&bars->o_full[x], 1);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == kLoadWarp) {
+    // ================================================================ loader
+    if (lane == 0) {
+      const uint64_t keep = policy_evict_last();   // K/V: re-read by other CTAs
+      const uint64_t once = policy_evict_first();  // Q: read by this CTA only
+      uint32_t q_bytes = 0;
+      for (int x = 0; x < 2; ++x) q_bytes += n_tiles[x] > 0 ? C::kTileBytes : 0;
+      mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+      for (int x = 0; x < 2; ++x) {
+        if (n_tiles[x] == 0) continue;
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_load_3d(sQ + x * C::kTileBytes + cb * C::kBlockBytes, &tmap_q, &bars->q_full, cb * 64,
+                      q0[x], b * p.H + h, once);
+      }
+      const int n_items = 2 * n_max;
+      int issued = 0;
+      for (int it = 0; it < n_items; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        if (!bounded_wait(&bars->kv_empty[st], ph ^ 1, abort_flag, p.status, kStatusTimeoutLoad))
+          break;
+        const CUtensorMap* map = (it & 1) ? &tmap_v : &tmap_k;
+        const int key0 = (it >> 1) * kBN;
+        mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_load_3d(sRing + st * C::kTileBytes + cb * C::kBlockBytes, map, &bars->kv_full[st],
+                      cb * 64, key0, b * p.Hkv + kvh, keep);
+        issued = it + 1;
+      }
+      // Drain: every copy this thread issued must have landed before exit.
+      bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutDrain);
+      for (int it = max(0, issued - C::kStages); it < issued; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        int dummy = 0;
+        // Ignore the abort flag here: wait for the copy itself (bounded).
+        bounded_wait(&bars->kv_full[st], ph, reinterpret_cast<volatile int*>(&dummy), p.status,
+                     kStatusTimeoutDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, kBM, kBN);
+      constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, kBM, D);
+      const uint32_t sQ_addr = smem_u32(sQ);
+      const uint32_t sRing_addr = smem_u32(sRing);
+      auto issue_qk = [&](int x, int st) {
+        const uint32_t d_tmem = tmem + x * kBN;
+        const uint32_t qa = sQ_addr + x * C::kTileBytes;
+        const uint32_t ka = sRing_addr + st * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::kBlockBytes + (kk % 4) * 32;
+          mma_f16_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                     kIdescQK, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int x, int st, bool accumulate) {
+        const uint32_t d_tmem = tmem + 2 * kBN + x * D;
+        const uint32_t p_tmem = tmem + x * kBN + kBN / 2;
+        const uint32_t va = sRing_addr + st * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          mma_f16_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, C::kBlockBytes, 1024),
+                     kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = n_max == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int itK = 2 * j;
+        const int stK = itK % C::kStages;
+        if (!(ok = bounded_wait(&bars->kv_full[stK], (itK / C::kStages) & 1, abort_flag, p.status,
+                                kStatusTimeoutMma)))
+          break;
+        tc_fence_after();
+        int stV = 0;
+        if (j > 0) {
+          const int itV = 2 * (j - 1) + 1;
+          stV = itV % C::kStages;
+          if (!(ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
+                                  kStatusTimeoutMma)))
+            break;
+          tc_fence_after();
+        }
+        for (int x = 0; x < 2; ++x) {
+          if (j > 0 && j - 1 < n_tiles[x]) {
+            if (!(ok = bounded_wait(&bars->p_full[x], (j - 1) & 1, abort_flag, p.status,
+                                    kStatusTimeoutMma)))
+              break;
+            tc_fence_after();
+            issue_pv(x, stV, j - 1 > 0);
+            if (j - 1 == n_tiles[x] - 1) mma_commit(&bars->o_full[x]);
+          }
+          if (j < n_tiles[x]) {
+            issue_qk(x, stK);
+            mma_commit(&bars->s_full[x]);
+          }
+        }
+        if (!ok) break;
+        if (j > 0) mma_commit(&bars->kv_empty[stV]);
+        mma_commit(&bars->kv_empty[stK]);
+      }
+      if (ok && n_max > 0) {
+        const int j = n_max - 1;
+        const int itV = 2 * j + 1;
+        const int stV = itV % C::kStages;
+        ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
+                          kStatusTimeoutMma);
+        if (ok) {
+          tc_fence_after();
+          for (int x = 0; x < 2; ++x) {
+            if (j < n_tiles[x]) {
+              if (!(ok = bounded_wait(&bars->p_full[x], j & 1, abort_flag, p.status,
+                                      kStatusTimeoutMma)))
+                break;
+              tc_fence_after();
+              issue_pv(x, stV, j > 0);
+              mma_commit(&bars->o_full[x]);
+            }
+          }
+          if (ok) mma_commit(&bars->kv_empty[stV]);
+        }
+      }
+      // Every MMA this thread issued must complete before TMEM is released.
+      mma_commit(&bars->mma_done);
+      int dummy = 0;
+      bounded_wait(&bars->mma_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status,
+                   kStatusTimeoutDrain);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax
+    const int x = warp / 4;     // 0 = tile H, 1 = tile L
+    const int wq = warp % 4;    // TMEM lane quarter owned by this warp
+    const int row = wq * 32 + lane;
+    const int q_row = q0[x] + row;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_tmem = tmem + lane_off + x * kBN;
+    const uint32_t o_tmem = tmem + lane_off + 2 * kBN + x * D;
+    const float lam = p.scale_log2;
+    float r = -INFINITY;  // retained reference, raw score units
+    float l = 0.f;
+    bool ok = true;
+    const int nt = n_tiles[x];
+
+    for (int j = 0; j < nt; ++j) {
+      ok = bounded_wait(&bars->s_full[x], j & 1, abort_flag, p.status, kStatusTimeoutSoftmax);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float s[kBN];
+      {
+        uint32_t u[32];
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          tmem_ld32(s_tmem + c * 32, u);
+          tmem_wait_ld();
+          reg_fence32(u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+        }
+      }
+      const int k0 = j * kBN;
+      const bool tail = k0 + kBN > p.Sk;
+      const bool diag = CAUSAL && (k0 + kBN - 1 > q0[x] + p.delta);
+      if (tail || diag) {
+        const int lim = CAUSAL ? min(p.Sk - 1, q_row + p.delta) : p.Sk - 1;  // last visible key
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (k0 + c > lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+
+      float gamma = 1.f;
+      if (j == 0) {
+        r = mx;
+      } else {
+        const float cand = fmaxf(r, mx);
+        if ((cand - r) * lam > kRescaleThreshold) {  // false when both are -inf
+          gamma = ex2_approx((r - cand) * lam);
+          r = cand;
+        }
+      }
+      if (j > 0 && __any_sync(0xffffffffu, gamma != 1.f)) {
+        // Correction: O_row *= gamma (warp-uniform path; gamma = 1 rows unchanged).
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(o_tmem + c * 32, u);
+          tmem_wait_ld();
+          reg_fence32(u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * gamma);
+          tmem_st32(o_tmem + c * 32, u);
+        }
+        tmem_wait_st();
+      }
+      l *= gamma;
+      const float rs = (r == -INFINITY) ? 0.f : r * lam;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) {
+        s[c] = ex2_approx(fmaf(s[c], lam, -rs));
+        sum += s[c];
+      }
+      l += sum;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1]);
+        tmem_st32(s_tmem + kBN / 2 + half * 32, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full[x]);
+    }
+
+    // ---- epilogue: O = O / l, LSE
+    if (q0[x] < p.Sq) {
+      bool have_o = false;
+      if (ok && nt > 0) {
+        have_o = bounded_wait(&bars->o_full[x], 0, abort_flag, p.status, kStatusTimeoutSoftmax);
+        have_o = __all_sync(0xffffffffu, have_o);
+        tc_fence_after();
+      }
+      const bool row_ok = q_row < p.Sq;
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      using T = uint16_t;
+      T* orow = reinterpret_cast<T*>(p.o) + ((static_cast<size_t>(b) * p.H + h) * p.Sq + (row_ok ? q_row : 0)) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (have_o) {
+          tmem_ld32(o_tmem + c * 32, u);
+          tmem_wait_ld();
+          reg_fence32(u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (row_ok && p.lse != nullptr) {
+        const float lse = (l > 0.f) ? (r * lam + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+        p.lse[(static_cast<size_t>(b) * p.H + h) * p.Sq + q_row] = lse;
+      }
+    }
+  }
+
+  // ---- teardown: all TMEM traffic done before the allocator warp frees it
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+template <int D, bool BF16, bool CAUSAL>
+int launch_t(const PrefillArgs& a) {
+  using C = Cfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_3d(&tq, a.q, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
+      !make_tmap_3d(&tk, a.k, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN) ||
+      !make_tmap_3d(&tv, a.v, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN))
+    return -1;
+  auto kern = prefill_fwd_kernel<D, BF16, CAUSAL>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+      return -1;
+    attr_set = true;
+  }
+  Params p;
+  p.o = a.o;
+  p.lse = a.lse;
+  p.B = a.B;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.Sq = a.Sq;
+  p.Sk = a.Sk;
+  p.g = a.H / a.Hkv;
+  p.n_pairs = (a.Sq + 2 * kBM - 1) / (2 * kBM);
+  p.delta = a.Sk - a.Sq;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.causal = CAUSAL ? 1 : 0;
+  p.status = a.status;
+  const long long grid = static_cast<long long>(a.B) * a.H * p.n_pairs;
+  if (grid > 0x7FFFFFFFLL) return -1;
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int launch_prefill(const PrefillArgs& a) {
+  if (a.d == 128) {
+    if (a.bf16) return a.causal ? launch_t<128, true, true>(a) : launch_t<128, true, false>(a);
+    return a.causal ? launch_t<128, false, true>(a) : launch_t<128, false, false>(a);
+  }
+  if (a.bf16) return a.causal ? launch_t<64, true, true>(a) : launch_t<64, true, false>(a);
+  return a.causal ? launch_t<64, false, true>(a) : launch_t<64, false, false>(a);
+}
+
+}  // namespace gbattn

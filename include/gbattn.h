@@ -1,0 +1,166 @@
+/*
+ * gbattn.h -- C ABI of libgbattn.so: exact tiled attention on GB300 (sm_103a).
+ *
+ * The library computes exact attention (no approximation):
+ *
+ *     O = softmax(scale * Q K^T + mask) V,      LSE = log sum_j exp(scale * q.k_j)
+ *
+ * as defined in M4.3 "IO-aware attention" 0x02A (scores, mask before the row
+ * normalisation, P V) and 0x09E (LSE = m + log l), with the grouped-query
+ * head map of M4.4 "FlashAttention-v2 decoding kernel boundary" 0x06A
+ * (kv_head = q_head / (H / Hkv)) and the causal predicate of M4.4 0x05.1A
+ * (key k visible to query q iff k <= q + (Sk - Sq), the bottom-right
+ * alignment of 0x05.1F).  The forward pass is a tiled online-softmax
+ * reduction over the key axis (M4.3 0x07-0x09; M4.4 0x03 Algorithm 1): the
+ * per-row (m, l, unnormalised O) state stays on chip and the [Sq, Sk] score
+ * and probability matrices never reach device memory.  Decode (one query per
+ * sequence) splits the key axis into chunks whose partial states are merged
+ * by rescale-and-add (M4.4 0x01 work-axis ledger, Flash-Decoding; M4.3 0x08B
+ * merge; M4.3 0x09E (LSE, O) form).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no device memory in any call, never frees caller memory, never
+ *    modifies inputs and never synchronises the stream: work is enqueued on
+ *    `stream` (a cudaStream_t; NULL = legacy default stream) and the call
+ *    returns immediately.
+ *  - Layout: every tensor is contiguous row-major [batch, heads, seq, d]
+ *    ("BHSD"); LSE is contiguous fp32 [batch, heads, seq].
+ *  - Pointers must be 16-byte aligned.  Element type of q/k/v/o is given by
+ *    `dtype` (GBATTN_F16 or GBATTN_BF16); arithmetic is fp32 with fp16/bf16
+ *    tensor-core operands; O is rounded to `dtype` (round-to-nearest-even).
+ *  - LSE is the natural-log sum of exp(scale * score) over the visible keys.
+ *    A query row with no visible key (only possible when causal and Sq > Sk)
+ *    gets O = 0 and LSE = -inf.
+ *  - Return value: GBATTN_OK or a negative GBATTN_E* code.  Argument errors
+ *    are detected on the host before anything is enqueued.  Asynchronous
+ *    device-side failures (a bounded wait inside a kernel that timed out) are
+ *    reported by gbattn_device_status() after the caller synchronises.
+ */
+#ifndef GBATTN_H_
+#define GBATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define GBATTN_OK 0
+#define GBATTN_EBADSHAPE (-1)       /* B, H, Hkv, Sq, Sk (or Sk_max) < 1, or a size overflows */
+#define GBATTN_EHEADS (-2)          /* H % Hkv != 0 (M4.4 0x06A admissibility) */
+#define GBATTN_EHEADDIM (-3)        /* d not in {64, 128} */
+#define GBATTN_EDTYPE (-4)          /* dtype is neither GBATTN_F16 nor GBATTN_BF16 */
+#define GBATTN_EPOINTER (-5)        /* a required pointer is NULL or not 16-byte aligned */
+#define GBATTN_EWORKSPACE (-6)      /* decode workspace smaller than attn_decode_workspace_bytes() */
+#define GBATTN_ELAUNCH (-7)         /* the CUDA runtime rejected a launch or a tensor map */
+#define GBATTN_EDEVICE_TIMEOUT (-8) /* a kernel's bounded wait gave up (gbattn_device_status) */
+#define GBATTN_ESPLIT (-9)          /* decode n_split < 1 or > 256 */
+#define GBATTN_EUNSUPPORTED (-10)   /* no sm_103a device, or the current device is not sm_103 */
+
+/* Element types of q/k/v/o. */
+#define GBATTN_F16 0
+#define GBATTN_BF16 1
+
+/*
+ * attn_fwd -- exact attention forward (prefill), tiled online softmax.
+ *
+ *   q     [B, H,   Sq, d]  dtype, input
+ *   k, v  [B, Hkv, Sk, d]  dtype, input (query head h reads KV head h / (H / Hkv))
+ *   o     [B, H,   Sq, d]  dtype, output
+ *   lse   [B, H,   Sq]     fp32, output; may be NULL (then not written)
+ *   scale multiplies the fp32 dot product before masking (usually 1/sqrt(d))
+ *   causal 0: every key visible; 1: key j visible to query i iff
+ *          j <= i + (Sk - Sq)
+ *
+ * Passages: M4.3 0x02A (definition), M4.3 0x09C-0x09E (unnormalised state,
+ * divide once, LSE), M4.4 0x03 Algorithm 1 (query-tile owner streams every
+ * visible key tile), M4.4 0x05.1B/0x05.1D (whole-future tiles skipped before
+ * Q K^T, partial tiles masked before the row maximum), M4.6 "FlashAttention
+ * hardware pipelines" 0x08-0x09 (two query tiles per CTA, TMEM score and
+ * output slots, conditional rescaling with threshold 8 in base-2 units).
+ *
+ * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM, EDTYPE, EPOINTER (q, k, v, o
+ * must be non-NULL; lse may be NULL), EUNSUPPORTED, ELAUNCH.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int H, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+             int dtype, void *stream);
+
+/*
+ * attn_decode_workspace_bytes -- bytes of device workspace attn_decode_splitkv
+ * needs: one fp32 partial state (m, l, o[d]) per (batch, query head, chunk),
+ * i.e. B * Hq * n_split * (d + 2) * 4.  Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int n_split, int d);
+
+/*
+ * attn_decode_splitkv -- one-query decode over a padded KV cache, split-KV.
+ *
+ *   q        [B, Hq, 1, d]        dtype, input
+ *   k_cache, v_cache [B, Hkv, Sk_max, d] dtype, input; rows >= seqlens[b] are
+ *            padding and are never read into the result (they may hold NaN)
+ *   seqlens  [B] int32 DEVICE array, 1 <= seqlens[b] <= Sk_max (values
+ *            outside that range are clamped into it on the device)
+ *   o        [B, Hq, 1, d]        dtype, output
+ *   lse      [B, Hq]              fp32, output; may be NULL
+ *   n_split  number of key chunks per sequence (1 .. 256); chunk c of
+ *            sequence b covers keys [floor(c*L_b/n_split), floor((c+1)*L_b/n_split))
+ *   workspace, workspace_bytes: caller-owned device scratch of at least
+ *            attn_decode_workspace_bytes(B, Hq, n_split, d) bytes, 16-byte
+ *            aligned; it receives the per-chunk partial states
+ *            ws[b][hq][c] = (m, l, o[0..d)) in natural-log units with
+ *            o unnormalised (o / l is the chunk's attention output); an empty
+ *            chunk is stored as the merge identity (m = -inf, l = 0, o = 0).
+ *
+ * Two kernels run in stream order: the partial kernel (one CTA per
+ * (chunk, KV head, batch) covering the H/Hkv query heads of that KV head,
+ * each K/V row read once) and the merge kernel (M4.3 0x08B common-maximum
+ * merge; final O = o / l, LSE = M + log l).
+ *
+ * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM, EDTYPE, EPOINTER, ESPLIT,
+ * EWORKSPACE, EUNSUPPORTED, ELAUNCH.
+ */
+int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
+                        const int *seqlens, void *o, float *lse,
+                        int B, int Hq, int Hkv, int Sk_max, int d, float scale,
+                        int n_split, void *workspace, size_t workspace_bytes,
+                        int dtype, void *stream);
+
+/*
+ * gbattn_causal_tile_counts -- host-only planning helper (no device work).
+ * Classifies the (ceil(Sq/Br) x ceil(Sk/Bc)) tile grid with the half-open
+ * ranges of M4.4 0x05.1A-B and delta = Sk - Sq:
+ *   skipped  : k0 > (q1 - 1) + delta        (whole tile in the future)
+ *   full     : (k1 - 1) <= q0 + delta       (no element mask needed)
+ *   partial  : otherwise                    (mask cells before the row max)
+ * Also returns the number of causally allowed cells and of cells inside
+ * visited (full + partial) tiles.  Any output pointer may be NULL.
+ * Returns GBATTN_OK or GBATTN_EBADSHAPE.
+ */
+int gbattn_causal_tile_counts(int Sq, int Sk, int Br, int Bc,
+                              long long *full, long long *partial, long long *skipped,
+                              long long *allowed_cells, long long *visited_cells);
+
+/*
+ * gbattn_device_status -- read and clear the library's device status word
+ * (synchronises the current device).  Returns GBATTN_OK, or
+ * GBATTN_EDEVICE_TIMEOUT if a kernel gave up a bounded wait since the last
+ * call, or GBATTN_ELAUNCH if the device reported an error.
+ */
+int gbattn_device_status(void);
+
+/* Text for a status code (static storage; never NULL). */
+const char *gbattn_error_string(int code);
+
+/* Library version string, e.g. "gbattn 0.1.0 sm_103a". */
+const char *gbattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBATTN_H_ */

@@ -1,0 +1,129 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, rejects bad arguments on the host before any launch, and its
+host-side causal tile planner reproduces the pages' tile-count fixtures."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from exact_tiled_attention_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load_library()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("defined",):
+                names.append(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("attn_fwd", "attn_decode_splitkv", "attn_decode_workspace_bytes"):
+        assert required in names
+    assert set(binding.EXPORTS) <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libgbattn.so does not export {name}"
+    assert lib.gbattn_version().decode().startswith("gbattn")
+
+
+def test_error_strings(lib):
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10]:
+        assert lib.gbattn_error_string(code)
+    assert lib.gbattn_error_string(12345) == b"unknown status code"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation rejects first
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=4, Hkv=2, Sq=8, Sk=8, d=64, scale=0.125,
+             causal=0, dtype=1, stream=None)
+    a.update(kw)
+    return lib.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"], a["Sq"],
+                        a["Sk"], a["d"], a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+def test_attn_fwd_validation(lib):
+    assert _fwd(lib, B=0) == -1
+    assert _fwd(lib, Sq=0) == -1
+    assert _fwd(lib, Sk=-3) == -1
+    assert _fwd(lib, H=4, Hkv=3) == -2
+    assert _fwd(lib, d=96) == -3
+    assert _fwd(lib, d=256) == -3
+    assert _fwd(lib, dtype=7) == -4
+    assert _fwd(lib, q=None) == -5
+    assert _fwd(lib, o=FAKE + 8) == -5
+    assert _fwd(lib, lse=FAKE + 2) == -5
+
+
+def _dec(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, Skm=64, d=128,
+             scale=0.1, n=4, ws=FAKE, wsb=1 << 20, dtype=1, stream=None)
+    a.update(kw)
+    return lib.attn_decode_splitkv(a["q"], a["k"], a["v"], a["sl"], a["o"], a["lse"], a["B"], a["Hq"],
+                                   a["Hkv"], a["Skm"], a["d"], a["scale"], a["n"], a["ws"], a["wsb"],
+                                   a["dtype"], a["stream"])
+
+
+def test_decode_validation(lib):
+    assert lib.attn_decode_workspace_bytes(64, 32, 16, 128) == 64 * 32 * 16 * 130 * 4
+    assert lib.attn_decode_workspace_bytes(0, 32, 16, 128) == 0
+    assert _dec(lib, B=0) == -1
+    assert _dec(lib, Hq=6, Hkv=4) == -2
+    assert _dec(lib, d=80) == -3
+    assert _dec(lib, dtype=3) == -4
+    assert _dec(lib, sl=None) == -5
+    assert _dec(lib, ws=None) == -5
+    assert _dec(lib, n=0) == -9
+    assert _dec(lib, n=257) == -9
+    need = lib.attn_decode_workspace_bytes(2, 8, 4, 128)
+    assert _dec(lib, wsb=need - 1) == -6
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_valid_call_without_gpu_is_refused(lib):
+    assert _fwd(lib) == -10
+
+
+def test_causal_tile_planner_matches_page_fixtures(lib, golden):
+    for case in golden("causal_tile_counts.json")["cases"]:
+        got = binding.gbattn_causal_tile_counts(case["Sq"], case["Sk"], case["Br"], case["Bc"])
+        assert (got["full"], got["partial"], got["skipped"]) == (case["full"], case["partial"],
+                                                                 case["skipped"])
+        if "allowed_cells" in case:
+            assert got["allowed_cells"] == case["allowed_cells"]
+        if "visited_cells" in case:
+            assert got["visited_cells"] == case["visited_cells"]
+        if "visited_tiles" in case:
+            assert got["full"] + got["partial"] == case["visited_tiles"]
+
+
+def test_causal_planner_bottom_right_rectangles(lib):
+    # Sq > Sk: early rows see nothing; allowed cells follow k <= q + (Sk - Sq).
+    got = binding.gbattn_causal_tile_counts(5, 2, 1, 1)
+    assert got["allowed_cells"] == 3  # rows 3 and 4 see 1 and 2 keys
+    got = binding.gbattn_causal_tile_counts(2, 5, 1, 1)
+    assert got["allowed_cells"] == 9
+    # the 8192-token causal prefill with 128 x 128 tiles visits 2,080 of 4,096 tiles
+    got = binding.gbattn_causal_tile_counts(8192, 8192, 128, 128)
+    assert got["full"] + got["partial"] == 2080 and got["partial"] == 64
