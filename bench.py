@@ -1,0 +1,559 @@
+"""Benchmark of the exact-attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gbattn|reference]
+                    [--workload prefill|decode]
+
+Default workload ("prefill"): the causal bf16 prefill forward, q/k/v
+[4, 16, 8192, 128], reported as attention TFLOP/s (4*B*H*Sq*Sk*d, halved for
+causal) against the measured dense bf16 tensor peak.  The split-KV decode
+workload (64 sequences x 32 query / 8 KV heads, 32768-slot bf16 cache, valid
+lengths uniform on [1024, 32768], 16 chunks) is measured in the same run and
+reported under "decode" (HBM GB/s of algorithmic bytes against the measured
+copy bandwidth); `--workload decode` makes it the headline instead.
+
+One step = one call of the hot path over one batch of resident synthetic
+input.  W warm-up steps, then exactly K steps timed with CUDA events on the
+launching stream, bracketed by a barrier and a device synchronize; the
+inputs (>= 512 MiB per step) exceed the 129 MB L2, so no flush is needed.
+Under torchrun every rank runs its own independent copy of the workload
+(weak scaling, no data-path collective); rank 0 prints one JSON line with the
+whole-job throughput (work of all ranks / max time over ranks).
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the baseline, not the target).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from exact_tiled_attention_gb300.inputs import WORKLOADS, make_workload  # noqa: E402
+
+PREFILL = WORKLOADS["causal_bf16_b4_h16_s8192_d128"]
+DECODE = WORKLOADS["decode_splitkv_bf16_b64_hq32_hkv8_sk32768_d128"]
+PREFILL_METRIC = "attention fwd TFLOP/s (% BF16 tensor peak)"
+DECODE_METRIC = "decode HBM GB/s (% peak)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- helpers
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_flops(w) -> float:
+    f = 4.0 * w.B * w.H * w.Sq * w.Sk * w.d
+    return f / 2 if w.causal else f
+
+
+def prefill_algorithmic_bytes(w) -> int:
+    e = 2  # bf16/fp16
+    return (w.B * w.H * w.Sq * w.d * e * 2          # Q read, O written
+            + 2 * w.B * w.Hkv * w.Sk * w.d * e      # K, V read once
+            + w.B * w.H * w.Sq * 4)                 # LSE written
+
+
+def decode_algorithmic_bytes(w, lens) -> int:
+    e = 2
+    kv = int(np.sum(lens)) * w.Hkv * w.d * e * 2                     # valid K and V rows once
+    partials = w.B * w.H * w.n_split * (w.d + 2) * 4 * 2              # written, then read by the merge
+    qo = w.B * w.H * w.d * e * 2 + w.B * w.H * 4 + w.B * 4             # q, O, LSE, lengths
+    return kv + partials + qo
+
+
+def kernel_source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+PREFILL_SOURCES = ["exact_tiled_attention_gb300/csrc/prefill_fwd.cu",
+                   "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]
+DECODE_SOURCES = ["exact_tiled_attention_gb300/csrc/decode_splitkv.cu",
+                  "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]
+
+
+def ncu_traffic(kernel_key: str, sources):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != kernel_source_hash(sources):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- GPU arm
+def time_steps(fn, steps, warmup, world, stream):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3  # seconds
+
+
+def bench_prefill(args, world, rank, peaks, peak_kind):
+    from exact_tiled_attention_gb300 import attn_fwd, gbattn_device_status
+
+    w = PREFILL
+    stream = torch.cuda.current_stream()
+    q, k, v = make_workload(w, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device="cuda")
+    run = lambda: attn_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)  # noqa: E731
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    secs = time_steps(run, args.steps, args.warmup, world, stream)
+    clocks = sampler.stop()
+    if gbattn_device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout")
+    secs = max_over_ranks(secs, world)
+    flops = prefill_flops(w)
+    tflops_job = flops * args.steps * world / secs / 1e12
+    per_launch = secs / args.steps
+    achieved = flops / per_launch / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = ncu_traffic("prefill_fwd_kernel<128,bf16,causal>", PREFILL_SOURCES)
+
+    # end to end through the public API: pinned host inputs copied in, O and
+    # LSE copied back, every step
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        attn_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    e2e_secs = max_over_ranks(time_steps(e2e_step, e2e_steps, 3, world, stream), world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": round(tflops_job, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(secs / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic i.i.d. N(0,1), seeded",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
+                   "d": w.d, "causal": w.causal, "flops_per_step": flops,
+                   "l2": "inputs 512 MiB per step > 129 MB L2; no flush",
+                   "parallelism": f"replicas x{world} (independent problems per GPU)"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": f"{peak_kind} bf16 burst",
+                     "frac_of_sustained": round(achieved / peaks.get("bf16_tflops_sustained", peak), 4),
+                     "algorithmic_bytes": prefill_algorithmic_bytes(w)},
+        "e2e": {"value": round(flops * e2e_steps * world / e2e_secs / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+def bench_decode(args, world, rank, peaks, peak_kind, steps=None, warmup=None):
+    from exact_tiled_attention_gb300 import attn_decode_splitkv, attn_decode_workspace_bytes, gbattn_device_status
+
+    steps = steps or args.steps
+    warmup = warmup if warmup is not None else args.warmup
+    w = DECODE
+    stream = torch.cuda.current_stream()
+    q, k, v, sl = make_workload(w, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(attn_decode_workspace_bytes(w.B, w.H, w.n_split, w.d), dtype=torch.uint8,
+                     device="cuda")
+    run = lambda: attn_decode_splitkv(q, k, v, sl, scale=w.scale, n_split=w.n_split, workspace=ws,  # noqa: E731
+                                      out=o, lse=lse, stream=stream)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    secs = time_steps(run, steps, warmup, world, stream)
+    clocks = sampler.stop()
+    if gbattn_device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout")
+    secs = max_over_ranks(secs, world)
+    lens = sl.cpu().numpy()
+    nbytes = decode_algorithmic_bytes(w, lens)
+    per_step = secs / steps
+    gbs_job = nbytes * steps * world / secs / 1e9
+    achieved = nbytes / per_step / 1e9
+    peak = peaks["hbm_gbs"]
+    traffic = ncu_traffic("decode_partial_kernel<128,bf16>", DECODE_SOURCES)
+
+    # end to end: only the step's inputs move each step (q and lengths in,
+    # O and LSE out); the KV cache is resident state, copied in once before.
+    hq = q.cpu().pin_memory()
+    hsl = sl.cpu().pin_memory()
+    ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    hl = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        sl.copy_(hsl, non_blocking=True)
+        attn_decode_splitkv(q, k, v, sl, scale=w.scale, n_split=w.n_split, workspace=ws, out=o, lse=lse,
+                            stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(steps, 20))
+    e2e_secs = max_over_ranks(time_steps(e2e_step, e2e_steps, 3, world, stream), world)
+    return {
+        "metric": DECODE_METRIC,
+        "value": round(gbs_job, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(per_step * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic i.i.d. N(0,1), seeded; lengths uniform on [1024, 32768]",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.H, "Hkv": w.Hkv, "Sk_max": w.Sk, "d": w.d,
+                   "n_split": w.n_split, "sum_valid_len": int(np.sum(lens)),
+                   "algorithmic_bytes_per_step": nbytes,
+                   "l2": "KV cache 8.6 GB > 129 MB L2; no flush",
+                   "parallelism": f"replicas x{world} (independent problems per GPU)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_kind": f"{peak_kind} copy bandwidth"},
+        "e2e": {"value": round(nbytes * e2e_steps * world / e2e_secs / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": hq.numel() * 2 + hsl.numel() * 4,
+                "d2h_bytes_per_step": ho.numel() * 2 + hl.numel() * 4},
+        "gpu_launches": 2 * steps,
+        "clocks": clocks,
+    }
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_prefill(target_seconds: float):
+    """Time the fp64 oracle on whole heads of the prefill workload (every
+    query row of each sampled (b, h) against its keys), as many heads as fit
+    in about target_seconds.  Returns (TFLOP/s, threads, sample description)."""
+    import oracle
+
+    w = PREFILL
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    q, k, v = make_workload(w, device=dev)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def run_heads(sel, n_rows=None):
+        t_total, cells = 0.0, 0.0
+        for (b, h) in sel:
+            kvh = h // (w.H // w.Hkv)
+            qh = q[b:b + 1, h:h + 1].float().cpu().numpy()
+            kh = k[b:b + 1, kvh:kvh + 1].float().cpu().numpy()
+            vh = v[b:b + 1, kvh:kvh + 1].float().cpu().numpy()
+            n = n_rows or w.Sq
+            rows = np.arange(w.Sq - n, w.Sq, dtype=np.int64)
+            t0 = time.perf_counter()
+            oracle.attn_fwd_rows(qh, kh, vh, w.scale, w.causal, rows)
+            t_total += time.perf_counter() - t0
+            vis = np.minimum(rows + 1 + (w.Sk - w.Sq), w.Sk) if w.causal else np.full(n, w.Sk)
+            cells += float(np.sum(np.maximum(vis, 0)))
+        return t_total, cells
+
+    dt, cells = run_heads(heads[:1], n_rows=512)
+    head_cells = float(w.Sq) * (w.Sk + 1) / 2 if w.causal else float(w.Sq) * w.Sk
+    t_head = dt / cells * head_cells
+    n_heads = int(min(len(heads), max(1, round(target_seconds / max(t_head, 1e-6)))))
+    dt, cells = run_heads(heads[:n_heads])
+    flops = 4.0 * w.d * cells
+    return flops / dt / 1e12, oracle.num_threads(), (
+        f"{n_heads} whole (b, h) heads of {w.B * w.H} (all {w.Sq} query rows each): "
+        f"{cells:.3e} visible cells, {dt:.1f} s")
+
+
+def cpu_oracle_decode(target_seconds: float):
+    import oracle
+
+    w = DECODE
+    q, k, v, sl = make_workload(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    lens = sl.cpu().numpy()
+    order = np.argsort(lens)
+    b = int(order[len(order) // 2])  # a median-length sequence
+    qb, kb, vb = (t[b:b + 1].float().cpu().numpy() for t in (q, k, v))
+    t0 = time.perf_counter()
+    oracle.attn_decode(qb, kb, vb, lens[b:b + 1], w.scale)
+    dt = time.perf_counter() - t0
+    reps = max(1, int(target_seconds / max(dt, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.attn_decode(qb, kb, vb, lens[b:b + 1], w.scale)
+    dt = time.perf_counter() - t0
+    nbytes = int(lens[b]) * w.Hkv * w.d * 2 * 2 * reps
+    return nbytes / dt / 1e9, oracle.num_threads(), (
+        f"sequence {b} (valid length {int(lens[b])}), all {w.H} query heads, {reps} repeats, {dt:.1f} s")
+
+
+def reference_arm(args, world):
+    """The fp64 oracle as it stands, timed on the host cores: every step is a
+    bounded sample of the workload (query rows of one head for prefill, one
+    sequence for decode), sized so the whole run takes about --cpu-seconds."""
+    import oracle
+
+    per_step = max(0.2, args.cpu_seconds / max(args.steps, 1))
+    if args.workload == "prefill":
+        w = PREFILL
+        q, k, v = make_workload(w, device="cuda" if torch.cuda.is_available() else "cpu")
+        qh, kh, vh = (t[0:1, 0:1].float().cpu().numpy() for t in (q, k, v))
+
+        def step(n):
+            rows = np.arange(w.Sq - n, w.Sq, dtype=np.int64)
+            t0 = time.perf_counter()
+            oracle.attn_fwd_rows(qh, kh, vh, w.scale, w.causal, rows)
+            return time.perf_counter() - t0, 4.0 * w.d * float(np.sum(rows + 1))
+
+        dt, work = step(32)
+        n = int(min(w.Sq, max(8, 32 * per_step / max(dt, 1e-6))))
+        unit, metric = "TFLOP/s", PREFILL_METRIC
+        scale_out = 1e12
+        sample = f"last {n} query rows of (b=0, h=0) against all {w.Sk} keys, causal"
+    else:
+        w = DECODE
+        q, k, v, sl = make_workload(w, device="cuda" if torch.cuda.is_available() else "cpu")
+        lens = sl.cpu().numpy()
+        b = int(np.argsort(lens)[len(lens) // 2])
+        qb, kb, vb = (t[b:b + 1].float().cpu().numpy() for t in (q, k, v))
+
+        def step(n):
+            t0 = time.perf_counter()
+            for _ in range(n):
+                oracle.attn_decode(qb, kb, vb, lens[b:b + 1], w.scale)
+            return time.perf_counter() - t0, float(n * int(lens[b]) * w.Hkv * w.d * 2 * 2)
+
+        dt, work = step(1)
+        n = int(max(1, per_step / max(dt, 1e-6)))
+        unit, metric = "GB/s", DECODE_METRIC
+        scale_out = 1e9
+        sample = (f"{n} decode(s) of sequence {b} (valid length {int(lens[b])}), all {w.H} query "
+                  f"heads; algorithmic K/V bytes")
+    for _ in range(args.warmup):
+        step(max(1, n // 8))
+    t_all = time.perf_counter()
+    rates = []
+    for _ in range(args.steps):
+        dt, work = step(n)
+        rates.append(work / dt / scale_out)
+    wall = time.perf_counter() - t_all
+    val = statistics.median(rates)
+    cores = oracle.num_threads()
+    return {"impl": "reference", "metric": metric, "value": val, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(wall / max(args.steps, 1) * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic i.i.d. N(0,1), seeded",
+            "config": {"workload": w.name, "sample_per_step": sample},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gbattn", "reference"], default="gbattn")
+    ap.add_argument("--workload", choices=["prefill", "decode"], default="prefill")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch size of both workloads (smaller cases for ncu captures)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup()
+    peaks, peak_kind = load_peaks()
+    if args.batch > 0:
+        import dataclasses
+
+        global PREFILL, DECODE
+        PREFILL = dataclasses.replace(PREFILL, B=args.batch)
+        DECODE = dataclasses.replace(DECODE, B=args.batch)
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args, world)), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
+
+    from exact_tiled_attention_gb300 import load_library
+
+    load_library()  # fail loudly if the CUDA library is missing
+    if args.workload == "prefill":
+        line = bench_prefill(args, world, rank, peaks, peak_kind)
+        if not args.no_secondary:
+            line["decode"] = bench_decode(args, world, rank, peaks, peak_kind,
+                                          steps=max(3, min(args.steps, 20)), warmup=3)
+    else:
+        line = bench_decode(args, world, rank, peaks, peak_kind)
+        if not args.no_secondary:
+            line["prefill"] = bench_prefill(args, world, rank, peaks, peak_kind)
+    torch.cuda.synchronize()
+    if rank == 0 and not args.no_cpu_baseline:
+        if args.workload == "prefill":
+            val, cores, sample = cpu_oracle_prefill(args.cpu_seconds)
+            line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                    "sample": sample}
+        else:
+            val, cores, sample = cpu_oracle_decode(args.cpu_seconds)
+            line["cpu_baseline"] = {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                    "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
