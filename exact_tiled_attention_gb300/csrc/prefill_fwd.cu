@@ -14,11 +14,15 @@
 //   O_L  [256+d,256+2d)     same for tile L
 // (M4.6 0x07 "Derive The Pinned Beta23 TMEM Map": 2N + 2 d_v <= 512.)
 //
-// Warp roles (320 threads):
-//   warps 0-3  softmax + correction + epilogue of tile H (thread = one row)
-//   warps 4-7  the same for tile L
-//   warp  8    TMEM allocation; lane 0 issues every tcgen05.mma and commit
-//   warp  9    lane 0 issues every TMA copy (Q once, then K_j, V_j)
+// Warp roles (384 threads = three warpgroups):
+//   warps 0-3   softmax + correction + epilogue of tile H (thread = one row)
+//   warps 4-7   the same for tile L
+//   warp  8     TMEM allocation; lane 0 issues every tcgen05.mma and commit
+//   warp  9     lane 0 issues every TMA copy (Q once, then K_j, V_j)
+//   warps 10-11 idle
+// Registers: launched at 168 per thread; the control warpgroup drops to 56
+// and the two softmax warpgroups rise to 224 (2*128*224 + 128*56 = 384*168),
+// enough to keep a whole 128-column score row in registers.
 //
 // MMA issue order (M4.6 0x08 startup / steady / drain):
 //   QK_H(0) QK_L(0) | PV_H(j-1) QK_H(j) PV_L(j-1) QK_L(j) ... | PV_H PV_L
@@ -47,7 +51,10 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxRegs = 224;
+constexpr int kControlRegs = 56;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units (fp16/bf16 row of M4.6 0x09 table)
@@ -69,6 +76,7 @@ struct Params {
   float* lse;
   int B, H, Hkv, Sq, Sk, g;
   int n_pairs;
+  int head_group;
   int delta;
   float scale_log2;
   int causal;
@@ -119,10 +127,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // ---- work unit: heaviest query pairs first (causal), heads fastest
+  // ---- work unit.  CTAs are ordered in groups of p.head_group (batch, head)
+  // pairs so that the K/V of the heads in flight stay resident in L2; inside
+  // a group the heaviest query pairs (most causal key tiles) come first and
+  // heads vary fastest (GQA heads sharing a KV head run side by side).
   const int BH = p.B * p.H;
-  const int bh = blockIdx.x % BH;
-  const int pair = p.n_pairs - 1 - blockIdx.x / BH;
+  const int group = blockIdx.x / (p.head_group * p.n_pairs);
+  const int heads_here = min(p.head_group, BH - group * p.head_group);
+  const int r_in = blockIdx.x - group * p.head_group * p.n_pairs;
+  const int bh = group * p.head_group + r_in % heads_here;
+  const int pair = p.n_pairs - 1 - r_in / heads_here;
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int kvh = h / p.g;
@@ -165,139 +179,145 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  if (warp == kLoadWarp) {
-    // ================================================================ loader
-    if (lane == 0) {
-      const uint64_t keep = policy_evict_last();   // K/V: re-read by other CTAs
-      const uint64_t once = policy_evict_first();  // Q: read by this CTA only
-      uint32_t q_bytes = 0;
-      for (int x = 0; x < 2; ++x) q_bytes += n_tiles[x] > 0 ? C::kTileBytes : 0;
-      mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-      for (int x = 0; x < 2; ++x) {
-        if (n_tiles[x] == 0) continue;
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d(sQ + x * C::kTileBytes + cb * C::kBlockBytes, &tmap_q, &bars->q_full, cb * 64,
-                      q0[x], b * p.H + h, once);
-      }
-      const int n_items = 2 * n_max;
-      int issued = 0;
-      for (int it = 0; it < n_items; ++it) {
-        const int st = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        if (!bounded_wait(&bars->kv_empty[st], ph ^ 1, abort_flag, p.status, kStatusTimeoutLoad))
-          break;
-        const CUtensorMap* map = (it & 1) ? &tmap_v : &tmap_k;
-        const int key0 = (it >> 1) * kBN;
-        mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
-        for (int cb = 0; cb < C::kColBlocks; ++cb)
-          tma_load_3d(sRing + st * C::kTileBytes + cb * C::kBlockBytes, map, &bars->kv_full[st],
-                      cb * 64, key0, b * p.Hkv + kvh, keep);
-        issued = it + 1;
-      }
-      // Drain: every copy this thread issued must have landed before exit.
-      bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutDrain);
-      for (int it = max(0, issued - C::kStages); it < issued; ++it) {
-        const int st = it % C::kStages;
-        const uint32_t ph = (it / C::kStages) & 1;
-        int dummy = 0;
-        // Ignore the abort flag here: wait for the copy itself (bounded).
-        bounded_wait(&bars->kv_full[st], ph, reinterpret_cast<volatile int*>(&dummy), p.status,
-                     kStatusTimeoutDrain);
-      }
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, kBM, kBN);
-      constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, kBM, D);
-      const uint32_t sQ_addr = smem_u32(sQ);
-      const uint32_t sRing_addr = smem_u32(sRing);
-      auto issue_qk = [&](int x, int st) {
-        const uint32_t d_tmem = tmem + x * kBN;
-        const uint32_t qa = sQ_addr + x * C::kTileBytes;
-        const uint32_t ka = sRing_addr + st * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kBlockBytes + (kk % 4) * 32;
-          mma_f16_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                     kIdescQK, kk > 0 ? 1u : 0u);
+  if (warp >= 8) {
+    // ---- control warpgroup: TMA loader and MMA issuer
+    regs_dec<kControlRegs>();
+    if (warp == kLoadWarp) {
+      // ================================================================ loader
+      if (lane == 0) {
+        const uint64_t keep = policy_evict_last();   // K/V: re-read by other CTAs
+        const uint64_t once = policy_evict_first();  // Q: read by this CTA only
+        uint32_t q_bytes = 0;
+        for (int x = 0; x < 2; ++x) q_bytes += n_tiles[x] > 0 ? C::kTileBytes : 0;
+        mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+        for (int x = 0; x < 2; ++x) {
+          if (n_tiles[x] == 0) continue;
+          for (int cb = 0; cb < C::kColBlocks; ++cb)
+            tma_load_3d(sQ + x * C::kTileBytes + cb * C::kBlockBytes, &tmap_q, &bars->q_full, cb * 64,
+                        q0[x], b * p.H + h, once);
         }
-      };
-      auto issue_pv = [&](int x, int st, bool accumulate) {
-        const uint32_t d_tmem = tmem + 2 * kBN + x * D;
-        const uint32_t p_tmem = tmem + x * kBN + kBN / 2;
-        const uint32_t va = sRing_addr + st * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_f16_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, C::kBlockBytes, 1024),
-                     kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+        const int n_items = 2 * n_max;
+        int issued = 0;
+        for (int it = 0; it < n_items; ++it) {
+          const int st = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (!bounded_wait(&bars->kv_empty[st], ph ^ 1, abort_flag, p.status, kStatusTimeoutLoad))
+            break;
+          const CUtensorMap* map = (it & 1) ? &tmap_v : &tmap_k;
+          const int key0 = (it >> 1) * kBN;
+          mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
+          for (int cb = 0; cb < C::kColBlocks; ++cb)
+            tma_load_3d(sRing + st * C::kTileBytes + cb * C::kBlockBytes, map, &bars->kv_full[st],
+                        cb * 64, key0, b * p.Hkv + kvh, keep);
+          issued = it + 1;
         }
-      };
-      bool ok = n_max == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int itK = 2 * j;
-        const int stK = itK % C::kStages;
-        if (!(ok = bounded_wait(&bars->kv_full[stK], (itK / C::kStages) & 1, abort_flag, p.status,
-                                kStatusTimeoutMma)))
-          break;
-        tc_fence_after();
-        int stV = 0;
-        if (j > 0) {
-          const int itV = 2 * (j - 1) + 1;
-          stV = itV % C::kStages;
-          if (!(ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
+        // Drain: every copy this thread issued must have landed before exit.
+        bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutDrain);
+        for (int it = max(0, issued - C::kStages); it < issued; ++it) {
+          const int st = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          int dummy = 0;
+          // Ignore the abort flag here: wait for the copy itself (bounded).
+          bounded_wait(&bars->kv_full[st], ph, reinterpret_cast<volatile int*>(&dummy), p.status,
+                       kStatusTimeoutDrain);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ================================================================ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, kBM, kBN);
+        constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, kBM, D);
+        const uint32_t sQ_addr = smem_u32(sQ);
+        const uint32_t sRing_addr = smem_u32(sRing);
+        auto issue_qk = [&](int x, int st) {
+          const uint32_t d_tmem = tmem + x * kBN;
+          const uint32_t qa = sQ_addr + x * C::kTileBytes;
+          const uint32_t ka = sRing_addr + st * C::kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * C::kBlockBytes + (kk % 4) * 32;
+            mma_f16_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                       kIdescQK, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto issue_pv = [&](int x, int st, bool accumulate) {
+          const uint32_t d_tmem = tmem + 2 * kBN + x * D;
+          const uint32_t p_tmem = tmem + x * kBN + kBN / 2;
+          const uint32_t va = sRing_addr + st * C::kTileBytes;
+  #pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            mma_f16_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, C::kBlockBytes, 1024),
+                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+          }
+        };
+        bool ok = n_max == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
+        for (int j = 0; ok && j < n_max; ++j) {
+          const int itK = 2 * j;
+          const int stK = itK % C::kStages;
+          if (!(ok = bounded_wait(&bars->kv_full[stK], (itK / C::kStages) & 1, abort_flag, p.status,
                                   kStatusTimeoutMma)))
             break;
           tc_fence_after();
-        }
-        for (int x = 0; x < 2; ++x) {
-          if (j > 0 && j - 1 < n_tiles[x]) {
-            if (!(ok = bounded_wait(&bars->p_full[x], (j - 1) & 1, abort_flag, p.status,
+          int stV = 0;
+          if (j > 0) {
+            const int itV = 2 * (j - 1) + 1;
+            stV = itV % C::kStages;
+            if (!(ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
                                     kStatusTimeoutMma)))
               break;
             tc_fence_after();
-            issue_pv(x, stV, j - 1 > 0);
-            if (j - 1 == n_tiles[x] - 1) mma_commit(&bars->o_full[x]);
           }
-          if (j < n_tiles[x]) {
-            issue_qk(x, stK);
-            mma_commit(&bars->s_full[x]);
-          }
-        }
-        if (!ok) break;
-        if (j > 0) mma_commit(&bars->kv_empty[stV]);
-        mma_commit(&bars->kv_empty[stK]);
-      }
-      if (ok && n_max > 0) {
-        const int j = n_max - 1;
-        const int itV = 2 * j + 1;
-        const int stV = itV % C::kStages;
-        ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
-                          kStatusTimeoutMma);
-        if (ok) {
-          tc_fence_after();
           for (int x = 0; x < 2; ++x) {
-            if (j < n_tiles[x]) {
-              if (!(ok = bounded_wait(&bars->p_full[x], j & 1, abort_flag, p.status,
+            if (j > 0 && j - 1 < n_tiles[x]) {
+              if (!(ok = bounded_wait(&bars->p_full[x], (j - 1) & 1, abort_flag, p.status,
                                       kStatusTimeoutMma)))
                 break;
               tc_fence_after();
-              issue_pv(x, stV, j > 0);
-              mma_commit(&bars->o_full[x]);
+              issue_pv(x, stV, j - 1 > 0);
+              if (j - 1 == n_tiles[x] - 1) mma_commit(&bars->o_full[x]);
+            }
+            if (j < n_tiles[x]) {
+              issue_qk(x, stK);
+              mma_commit(&bars->s_full[x]);
             }
           }
-          if (ok) mma_commit(&bars->kv_empty[stV]);
+          if (!ok) break;
+          if (j > 0) mma_commit(&bars->kv_empty[stV]);
+          mma_commit(&bars->kv_empty[stK]);
         }
+        if (ok && n_max > 0) {
+          const int j = n_max - 1;
+          const int itV = 2 * j + 1;
+          const int stV = itV % C::kStages;
+          ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
+                            kStatusTimeoutMma);
+          if (ok) {
+            tc_fence_after();
+            for (int x = 0; x < 2; ++x) {
+              if (j < n_tiles[x]) {
+                if (!(ok = bounded_wait(&bars->p_full[x], j & 1, abort_flag, p.status,
+                                        kStatusTimeoutMma)))
+                  break;
+                tc_fence_after();
+                issue_pv(x, stV, j > 0);
+                mma_commit(&bars->o_full[x]);
+              }
+            }
+            if (ok) mma_commit(&bars->kv_empty[stV]);
+          }
+        }
+        // Every MMA this thread issued must complete before TMEM is released.
+        mma_commit(&bars->mma_done);
+        int dummy = 0;
+        bounded_wait(&bars->mma_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status,
+                     kStatusTimeoutDrain);
       }
-      // Every MMA this thread issued must complete before TMEM is released.
-      mma_commit(&bars->mma_done);
-      int dummy = 0;
-      bounded_wait(&bars->mma_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status,
-                   kStatusTimeoutDrain);
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    // ---- softmax warpgroups
+    regs_inc<kSoftmaxRegs>();
     // ================================================================ softmax
     const int x = warp / 4;     // 0 = tile H, 1 = tile L
     const int wq = warp % 4;    // TMEM lane quarter owned by this warp
@@ -319,18 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      float s[kBN];
-      {
-        uint32_t u[32];
+      // ---- S row -> registers (four loads in flight, one wait)
+      uint32_t u[kBN];
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          tmem_ld32(s_tmem + c * 32, u);
-          tmem_wait_ld();
-          reg_fence32(u);
+      for (int c = 0; c < kBN / 32; ++c)
+        tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+      tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
-        }
-      }
+      for (int c = 0; c < kBN / 32; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+      float* s = reinterpret_cast<float*>(u);
       const int k0 = j * kBN;
       const bool tail = k0 + kBN > p.Sk;
       const bool diag = CAUSAL && (k0 + kBN - 1 > q0[x] + p.delta);
@@ -340,9 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN; ++c)
           if (k0 + c > lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // ---- row maximum: eight independent three-input max chains
+      float mx8[8];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i < kBN ? c + 8 + i : c + i]);
+      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                             fmaxf(mx8[6], mx8[7]));
 
       float gamma = 1.f;
       if (j == 0) {
@@ -354,35 +378,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           r = cand;
         }
       }
-      if (j > 0 && __any_sync(0xffffffffu, gamma != 1.f)) {
-        // Correction: O_row *= gamma (warp-uniform path; gamma = 1 rows unchanged).
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(o_tmem + c * 32, u);
-          tmem_wait_ld();
-          reg_fence32(u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * gamma);
-          tmem_st32(o_tmem + c * 32, u);
-        }
-        tmem_wait_st();
-      }
       l *= gamma;
+      // ---- P = 2^(lambda*s - lambda*r), row sum, pack to 16 bits, store to TMEM
       const float rs = (r == -INFINITY) ? 0.f : r * lam;
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        s[c] = ex2_approx(fmaf(s[c], lam, -rs));
-        sum += s[c];
-      }
-      l += sum;
+      const float2 lam2 = make_float2(lam, lam);
+      const float2 nrs2 = make_float2(-rs, -rs);
+      float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(s[half * 64 + 2 * i], s[half * 64 + 2 * i + 1]);
+        for (int i = 0; i < 32; ++i) {
+          const int c = half * 64 + 2 * i;
+          float2 t = ffma2(make_float2(s[c], s[c + 1]), lam2, nrs2);
+          t.x = ex2_approx(t.x);
+          t.y = ex2_approx(t.y);
+          sum4[i & 3] = fadd2(sum4[i & 3], t);
+          pk[i] = pack2<BF16>(t.x, t.y);
+        }
         tmem_st32(s_tmem + kBN / 2 + half * 32, pk);
+      }
+      const float2 s01 = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
+      l += s01.x + s01.y;
+      // ---- correction: O_row *= gamma once the scores are dead (warp-uniform
+      // path; rows whose reference did not move carry gamma = 1)
+      if (j > 0 && __any_sync(0xffffffffu, gamma != 1.f)) {
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t w32[32];
+          tmem_ld32(o_tmem + c * 32, w32);
+          tmem_wait_ld();
+          reg_fence32(w32);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w32[i] = __float_as_uint(__uint_as_float(w32[i]) * gamma);
+          tmem_st32(o_tmem + c * 32, w32);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -462,6 +493,15 @@ int launch_t(const PrefillArgs& a) {
   p.Sk = a.Sk;
   p.g = a.H / a.Hkv;
   p.n_pairs = (a.Sq + 2 * kBM - 1) / (2 * kBM);
+  {
+    // Heads per scheduling group: about 48 MB of K/V in flight (L2 is 129 MB).
+    const long long kv_head_bytes = 4LL * a.Sk * D;  // K and V, 16-bit
+    long long kv_heads = (48LL << 20) / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+    if (kv_heads < 1) kv_heads = 1;
+    long long hg = kv_heads * p.g;
+    const long long BH = static_cast<long long>(a.B) * a.H;
+    p.head_group = static_cast<int>(hg < BH ? hg : BH);
+  }
   p.delta = a.Sk - a.Sq;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.causal = CAUSAL ? 1 : 0;
