@@ -18,7 +18,7 @@
 // (M4.3 0x08B with the 0x08C validity branch): M = max m_c,
 // l = sum e^(m_c - M) l_c, o = sum e^(m_c - M) o_c; O = o / l,
 // LSE = M + log l.  This is the split-KV tower's outer bracket ("Learning
-// FlashAttention the Hard Way, Part 2", Move 6; M4.4 0x01 Flash-Decoding).
+// FlashAttention the Hard Way — Part 2", Move 6; M4.4 0x01 Flash-Decoding).
 #include <cuda_runtime.h>
 
 #include "gbattn_internal.h"

@@ -7,7 +7,7 @@ GPU tests and the oracle consume the SAME rounded tensors.
 
 The shapes are those of the workloads the pages discuss: a tiny fp16 forward,
 the [1, 8, 4096, 64] fp16 non-causal shape timed in "Learning FlashAttention
-the Hard Way, Part 2", a causal bf16 [4, 16, 8192, 128] prefill, a GQA causal
+the Hard Way — Part 2", a causal bf16 [4, 16, 8192, 128] prefill, a GQA causal
 prefill (32 query heads over 8 KV heads) and a 64-sequence one-query decode
 over a 32768-slot KV cache split into 16 chunks.
 """

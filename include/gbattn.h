@@ -5,9 +5,9 @@
  *
  *     O = softmax(scale * Q K^T + mask) V,      LSE = log sum_j exp(scale * q.k_j)
  *
- * as defined in M4.3 "IO-aware attention" 0x02A (scores, mask before the row
+ * as defined in M4.3 "IO-Aware Attention and FlashAttention-1" 0x02A (scores, mask before the row
  * normalisation, P V) and 0x09E (LSE = m + log l), with the grouped-query
- * head map of M4.4 "FlashAttention-v2 decoding kernel boundary" 0x06A
+ * head map of M4.4 "FlashAttention-2 Work Partitioning and the Decode Boundary" 0x06A
  * (kv_head = q_head / (H / Hkv)) and the causal predicate of M4.4 0x05.1A
  * (key k visible to query q iff k <= q + (Sk - Sq), the bottom-right
  * alignment of 0x05.1F).  The forward pass is a tiled online-softmax
@@ -79,8 +79,8 @@ extern "C" {
  * Passages: M4.3 0x02A (definition), M4.3 0x09C-0x09E (unnormalised state,
  * divide once, LSE), M4.4 0x03 Algorithm 1 (query-tile owner streams every
  * visible key tile), M4.4 0x05.1B/0x05.1D (whole-future tiles skipped before
- * Q K^T, partial tiles masked before the row maximum), M4.6 "FlashAttention
- * hardware pipelines" 0x08-0x09 (two query tiles per CTA, TMEM score and
+ * Q K^T, partial tiles masked before the row maximum), M4.6 "FlashAttention-3/4
+ * Hardware Pipelines" 0x08-0x09 (two query tiles per CTA, TMEM score and
  * output slots, conditional rescaling with threshold 8 in base-2 units).
  *
  * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM, EDTYPE, EPOINTER (q, k, v, o
@@ -111,10 +111,13 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int n_split, int d);
  *            sequence b covers keys [floor(c*L_b/n_split), floor((c+1)*L_b/n_split))
  *   workspace, workspace_bytes: caller-owned device scratch of at least
  *            attn_decode_workspace_bytes(B, Hq, n_split, d) bytes, 16-byte
- *            aligned; it receives the per-chunk partial states
- *            ws[b][hq][c] = (m, l, o[0..d)) in natural-log units with
- *            o unnormalised (o / l is the chunk's attention output); an empty
- *            chunk is stored as the merge identity (m = -inf, l = 0, o = 0).
+ *            aligned; it receives the per-chunk partial states, in
+ *            natural-log units, as two consecutive fp32 arrays:
+ *              o_part [B, Hq, n_split, d]  unnormalised o (o / l is the
+ *                                          chunk's attention output)
+ *              ml_part[B, Hq, n_split, 2]  (m, l)
+ *            an empty chunk is stored as the merge identity
+ *            (m = -inf, l = 0, o = 0).
  *
  * Two kernels run in stream order: the partial kernel (one CTA per
  * (chunk, KV head, batch) covering the H/Hkv query heads of that KV head,

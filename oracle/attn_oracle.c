@@ -10,14 +10,15 @@
  * What it computes is the definition, written out with no tiling, no
  * streaming and no reordering beyond "for every row, for every key":
  *
- *   M4.3 "IO-aware attention", 0x02A (the semantic graph):
+ *   M4.3 "IO-Aware Attention and FlashAttention-1", 0x02A (the semantic graph):
  *       S_raw[b,h,i,j] = tau * <Q[b,h,i,:], K[b,g(h),j,:]>
  *       S = mask(S_raw)                       (mask before row normalisation)
  *       P = softmax_row(S),  O = P V
  *   M4.3 0x06B (safe softmax): m = max_j s_j, l = sum_j exp(s_j - m)
  *   M4.3 0x09A / 0x09E: O = u / l with u = sum_j exp(s_j - m) v_j,
  *                       LSE = m + log(l)
- *   M4.4 "FlashAttention-2 ... decoding kernel boundary", 0x06A (GQA):
+ *   M4.4 "FlashAttention-2 Work Partitioning and the Decode Boundary",
+ *       0x06A (GQA):
  *       g = H_q / H_kv, kv_head = q_head / g  (integer division)
  *   M4.4 0x05.1A / 0x05.1F (causal):
  *       visible(q, k) iff k <= q + delta, delta = S_k - S_q (bottom-right)

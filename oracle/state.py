@@ -5,7 +5,7 @@ the bench's CPU-baseline leg use it to check the CUDA kernels' partial states
 and to pin the oracle against the worked traces the pages print.
 
 Sources (page, section):
-  M4.3 "IO-aware attention" 0x08A  state(A) = (m, l, u, n) of an index set
+  M4.3 "IO-Aware Attention and FlashAttention-1" 0x08A  state(A) = (m, l, u, n) of an index set
   M4.3 0x08B                       binary merge with one common maximum
   M4.3 0x08C                       identity (-inf, 0, 0, 0) with a validity flag
   M4.3 0x09A / 0x09E               O = u / l,  LSE = m + log l
