@@ -60,6 +60,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, sz,
                                             ci, vp]
         lib.attn_decode_splitkv.restype = ci
+        lib.attn_decode_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci,
+                                                    ci, vp]
+        lib.attn_decode_splitkv_noalloc.restype = ci
+        lib.attn_decode_noalloc_scratch_bytes.argtypes = []
+        lib.attn_decode_noalloc_scratch_bytes.restype = sz
         lib.gbattn_causal_tile_counts.argtypes = [ci, ci, ci, ci, ll_p, ll_p, ll_p, ll_p, ll_p]
         lib.gbattn_causal_tile_counts.restype = ci
         lib.gbattn_device_status.argtypes = []
@@ -180,6 +185,34 @@ def attn_decode_splitkv(q, k_cache, v_cache, seqlens, scale: float | None = None
     if rc != GBATTN_OK:
         raise GbattnError(rc, "attn_decode_splitkv")
     return out, lse, workspace
+
+
+def attn_decode_splitkv_noalloc(q, k_cache, v_cache, seqlens, scale: float | None = None,
+                                n_split: int = 16, out=None, lse=None, return_lse: bool = True,
+                                stream=None):
+    """attn_decode_splitkv without a workspace argument, for callers that
+    cannot allocate device memory: the partial states go to the library's
+    fixed 32 MiB device array (shared by all calls; order overlapping calls).
+    Outputs are allocated here only when `out`/`lse` are not given."""
+    _check(q, "q", 4)
+    _check(k_cache, "k_cache", 4)
+    _check(v_cache, "v_cache", 4)
+    B, Hq, _, d = q.shape
+    Hkv, Sk_max = k_cache.shape[1], k_cache.shape[2]
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    rc = load_library().attn_decode_splitkv_noalloc(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seqlens.data_ptr(), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, B, Hq, Hkv, Sk_max, d, float(scale),
+        int(n_split), dt, _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "attn_decode_splitkv_noalloc")
+    return out, lse
 
 
 def gbattn_causal_tile_counts(Sq: int, Sk: int, Br: int, Bc: int) -> dict:

@@ -134,6 +134,35 @@ int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
                         int dtype, void *stream);
 
 /*
+ * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot
+ * allocate device memory (a host framework that owns every allocation and
+ * forbids plugins from calling cudaMalloc, memory-capped or real-time
+ * services that must not enter the allocator, C callers that only receive
+ * their input and output pointers).  The pages have no counterpart: this is
+ * a packaging variant of the split-KV decode above, not part of the method.
+ *
+ * Arguments and results are those of attn_decode_splitkv without the
+ * workspace pair: the partial states go to a fixed array inside the library
+ * (attn_decode_noalloc_scratch_bytes() = 32 MiB, held by every GPU that loads
+ * the library until the process exits).  Problems whose
+ * attn_decode_workspace_bytes(B, Hq, n_split, d) exceeds that size return
+ * GBATTN_EWORKSPACE before any device work.  The call allocates nothing.
+ *
+ * The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * Every call shares the array (nothing in it needs clearing: each call
+ * overwrites the states it reads), so two calls whose kernels may overlap on
+ * the GPU race and must be ordered by the caller.
+ */
+int attn_decode_splitkv_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                const int *seqlens, void *o, float *lse,
+                                int B, int Hq, int Hkv, int Sk_max, int d, float scale,
+                                int n_split, int dtype, void *stream);
+
+/* Bytes of the fixed scratch array used by attn_decode_splitkv_noalloc. */
+size_t attn_decode_noalloc_scratch_bytes(void);
+
+/*
  * gbattn_causal_tile_counts -- host-only planning helper (no device work).
  * Classifies the (ceil(Sq/Br) x ceil(Sk/Bc)) tile grid with the half-open
  * ranges of M4.4 0x05.1A-B and delta = Sk - Sq:
