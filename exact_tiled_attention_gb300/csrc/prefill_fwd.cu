@@ -140,14 +140,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int kvh = h / p.g;
-  int n_tiles[2];
-  int q0[2];
-#pragma unroll
-  for (int x = 0; x < 2; ++x) {
-    q0[x] = pair * 2 * kBM + x * kBM;
-    n_tiles[x] = tiles_for(q0[x], p.Sq, p.Sk, CAUSAL ? 1 : 0, p.delta);
-  }
-  const int n_max = max(n_tiles[0], n_tiles[1]);
+  // Per-tile first query row and key-tile count (scalars, not arrays: the
+  // roles index them with a runtime tile number).
+  const int q0_h = pair * 2 * kBM, q0_l = q0_h + kBM;
+  const int nt_h = tiles_for(q0_h, p.Sq, p.Sk, CAUSAL ? 1 : 0, p.delta);
+  const int nt_l = tiles_for(q0_l, p.Sq, p.Sk, CAUSAL ? 1 : 0, p.delta);
+  const int n_max = max(nt_h, nt_l);
 
   // ---- setup
   if (threadIdx.x == 0) {
@@ -188,13 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t keep = policy_evict_last();   // K/V: re-read by other CTAs
         const uint64_t once = policy_evict_first();  // Q: read by this CTA only
         uint32_t q_bytes = 0;
-        for (int x = 0; x < 2; ++x) q_bytes += n_tiles[x] > 0 ? C::kTileBytes : 0;
+        q_bytes += nt_h > 0 ? C::kTileBytes : 0;
+        q_bytes += nt_l > 0 ? C::kTileBytes : 0;
         mbar_arrive_expect_tx(&bars->q_full, q_bytes);
         for (int x = 0; x < 2; ++x) {
-          if (n_tiles[x] == 0) continue;
+          if ((x ? nt_l : nt_h) == 0) continue;
           for (int cb = 0; cb < C::kColBlocks; ++cb)
             tma_load_3d(sQ + x * C::kTileBytes + cb * C::kBlockBytes, &tmap_q, &bars->q_full, cb * 64,
-                        q0[x], b * p.H + h, once);
+                        x ? q0_l : q0_h, b * p.H + h, once);
         }
         const int n_items = 2 * n_max;
         int issued = 0;
@@ -225,87 +224,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ================================================================ MMA issuer
+      // One thread issues both tiles' MMAs, which keeps the two tiles
+      // alternating on the tensor pipe (H's softmax overlaps L's MMAs and
+      // vice versa).  Step j waits for K_j and V_{j-1} first (normally landed
+      // long before), then for each tile's P, so PV and QK issue back to back.
       if (lane == 0) {
         constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, kBM, kBN);
         constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, kBM, D);
-        const uint32_t sQ_addr = smem_u32(sQ);
-        const uint32_t sRing_addr = smem_u32(sRing);
+        const uint32_t ring_addr = smem_u32(sRing);
+        // Descriptors are built once; a K-step only adds (byte offset >> 4)
+        // to the start-address field (every offset stays inside its tile).
+        const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
         auto issue_qk = [&](int x, int st) {
-          const uint32_t d_tmem = tmem + x * kBN;
-          const uint32_t qa = sQ_addr + x * C::kTileBytes;
-          const uint32_t ka = sRing_addr + st * C::kTileBytes;
-  #pragma unroll
+          const uint64_t qd = q_desc + ((x * C::kTileBytes) >> 4);
+          const uint64_t kd = smem_desc_sw128(ring_addr + st * C::kTileBytes, 16, 1024);
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * C::kBlockBytes + (kk % 4) * 32;
-            mma_f16_ss(d_tmem, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                       kIdescQK, kk > 0 ? 1u : 0u);
+            const uint64_t off = ((kk / 4) * C::kBlockBytes + (kk % 4) * 32) >> 4;
+            mma_f16_ss(tmem + x * kBN, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
         };
         auto issue_pv = [&](int x, int st, bool accumulate) {
-          const uint32_t d_tmem = tmem + 2 * kBN + x * D;
-          const uint32_t p_tmem = tmem + x * kBN + kBN / 2;
-          const uint32_t va = sRing_addr + st * C::kTileBytes;
-  #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            mma_f16_ts(d_tmem, p_tmem + kk * 8, smem_desc_sw128(va + kk * 2048, C::kBlockBytes, 1024),
+          const uint64_t vd = smem_desc_sw128(ring_addr + st * C::kTileBytes, C::kBlockBytes, 1024);
+          const uint32_t s_col = tmem + x * kBN;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_f16_ts(tmem + 2 * kBN + x * D, s_col + kBN / 2 + kk * 8, vd + ((kk * 2048) >> 4),
                        kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-          }
         };
         bool ok = n_max == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
-        for (int j = 0; ok && j < n_max; ++j) {
-          const int itK = 2 * j;
-          const int stK = itK % C::kStages;
-          if (!(ok = bounded_wait(&bars->kv_full[stK], (itK / C::kStages) & 1, abort_flag, p.status,
-                                  kStatusTimeoutMma)))
+        // Step j issues PV_X(j-1) then QK_X(j) for X = H, L; step n_max drains.
+        for (int j = 0; ok && j <= n_max; ++j) {
+          const bool have_v = j > 0, have_k = j < n_max;
+          const int itK = 2 * j, itV = 2 * j - 1;
+          const int stK = itK % C::kStages, stV = have_v ? itV % C::kStages : 0;
+          if (have_k && !(ok = bounded_wait(&bars->kv_full[stK], (itK / C::kStages) & 1, abort_flag,
+                                            p.status, kStatusTimeoutMma)))
             break;
-          tc_fence_after();
-          int stV = 0;
-          if (j > 0) {
-            const int itV = 2 * (j - 1) + 1;
-            stV = itV % C::kStages;
-            if (!(ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
-                                    kStatusTimeoutMma)))
-              break;
-            tc_fence_after();
-          }
+          if (have_v && !(ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag,
+                                            p.status, kStatusTimeoutMma)))
+            break;
+#pragma unroll
           for (int x = 0; x < 2; ++x) {
-            if (j > 0 && j - 1 < n_tiles[x]) {
+            const int nt = x ? nt_l : nt_h;
+            if (have_v && j - 1 < nt) {
               if (!(ok = bounded_wait(&bars->p_full[x], (j - 1) & 1, abort_flag, p.status,
                                       kStatusTimeoutMma)))
                 break;
               tc_fence_after();
               issue_pv(x, stV, j - 1 > 0);
-              if (j - 1 == n_tiles[x] - 1) mma_commit(&bars->o_full[x]);
+              if (j - 1 == nt - 1) mma_commit(&bars->o_full[x]);
             }
-            if (j < n_tiles[x]) {
+            if (have_k && j < nt) {
               issue_qk(x, stK);
               mma_commit(&bars->s_full[x]);
             }
           }
           if (!ok) break;
-          if (j > 0) mma_commit(&bars->kv_empty[stV]);
-          mma_commit(&bars->kv_empty[stK]);
-        }
-        if (ok && n_max > 0) {
-          const int j = n_max - 1;
-          const int itV = 2 * j + 1;
-          const int stV = itV % C::kStages;
-          ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag, p.status,
-                            kStatusTimeoutMma);
-          if (ok) {
-            tc_fence_after();
-            for (int x = 0; x < 2; ++x) {
-              if (j < n_tiles[x]) {
-                if (!(ok = bounded_wait(&bars->p_full[x], j & 1, abort_flag, p.status,
-                                        kStatusTimeoutMma)))
-                  break;
-                tc_fence_after();
-                issue_pv(x, stV, j > 0);
-                mma_commit(&bars->o_full[x]);
-              }
-            }
-            if (ok) mma_commit(&bars->kv_empty[stV]);
-          }
+          if (have_v) mma_commit(&bars->kv_empty[stV]);
+          if (have_k) mma_commit(&bars->kv_empty[stK]);
         }
         // Every MMA this thread issued must complete before TMEM is released.
         mma_commit(&bars->mma_done);
@@ -322,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = warp / 4;     // 0 = tile H, 1 = tile L
     const int wq = warp % 4;    // TMEM lane quarter owned by this warp
     const int row = wq * 32 + lane;
-    const int q_row = q0[x] + row;
+    const int q0x = x ? q0_l : q0_h;
+    const int q_row = q0x + row;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + x * kBN;
     const uint32_t o_tmem = tmem + lane_off + 2 * kBN + x * D;
@@ -330,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float r = -INFINITY;  // retained reference, raw score units
     float l = 0.f;
     bool ok = true;
-    const int nt = n_tiles[x];
+    const int nt = x ? nt_l : nt_h;
 
     for (int j = 0; j < nt; ++j) {
       ok = bounded_wait(&bars->s_full[x], j & 1, abort_flag, p.status, kStatusTimeoutSoftmax);
@@ -350,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float* s = reinterpret_cast<float*>(u);
       const int k0 = j * kBN;
       const bool tail = k0 + kBN > p.Sk;
-      const bool diag = CAUSAL && (k0 + kBN - 1 > q0[x] + p.delta);
+      const bool diag = CAUSAL && (k0 + kBN - 1 > q0x + p.delta);
       if (tail || diag) {
         const int lim = CAUSAL ? min(p.Sk - 1, q_row + p.delta) : p.Sk - 1;  // last visible key
 #pragma unroll
@@ -421,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---- epilogue: O = O / l, LSE
-    if (q0[x] < p.Sq) {
+    if (q0x < p.Sq) {
       bool have_o = false;
       if (ok && nt > 0) {
         have_o = bounded_wait(&bars->o_full[x], 0, abort_flag, p.status, kStatusTimeoutSoftmax);
