@@ -5,29 +5,40 @@
 // "L" = the next 128 rows) of one (batch, query head) and streams every
 // visible 128-key K/V tile of that head's KV head once for both query tiles
 // (M4.4 0x03 Algorithm 1: query-tile owner; M4.6 0x08: two query tiles per
-// CTA so one tile's softmax overlaps the other tile's tensor-core work).
+// CTA share each K/V tile).
 //
-// Tensor memory map (512 columns, 128 lanes; lane = query row of the tile):
-//   S_H  [  0,128)  fp32 scores of tile H;  P_H (16-bit) aliases [ 64,128)
-//   S_L  [128,256)  fp32 scores of tile L;  P_L (16-bit) aliases [192,256)
-//   O_H  [256,256+d)        unnormalised output accumulator of tile H
-//   O_L  [256+d,256+2d)     same for tile L
-// (M4.6 0x07 "Derive The Pinned Beta23 TMEM Map": 2N + 2 d_v <= 512.)
+// Tensor memory (512 columns, 128 lanes; lane = query row of the tile):
+//   S_H  [  0,128)  fp32 scores of tile H      S_L  [128,256)  of tile L
+//   O_H  [256,256+d)  unnormalised output      O_L  [256+d,256+2d)
+// (the M4.6 0x07 capacity rule 2N + 2 d_v <= 512).
+//
+// Shared memory: Q_H, Q_L; P_H, P_L (16-bit probabilities, K-major with the
+// 128-byte swizzle, the A operand of the P.V MMA); a ring of K/V slots.
+//
+// Why P lives in shared memory: with P aliased into its S columns (the
+// pages' FA4 map), QK(j+1) may only start after PV(j) has read P(j), so
+// every tile's softmax sits on the critical path of the tensor pipe.  With
+// P in its own buffer, QK_X(j+1) is issued as soon as the softmax threads
+// have copied S_X(j) into registers; each tile's softmax then runs back to
+// back and the tensor pipe, fed by both tiles, is the bound.
 //
 // Warp roles (384 threads = three warpgroups):
 //   warps 0-3   softmax + correction + epilogue of tile H (thread = one row)
 //   warps 4-7   the same for tile L
-//   warp  8     TMEM allocation; lane 0 issues every tcgen05.mma and commit
-//   warp  9     lane 0 issues every TMA copy (Q once, then K_j, V_j)
-//   warps 10-11 idle
+//   warp  8     TMEM allocation; lane 0 issues tile H's MMAs and commits
+//   warp  9     lane 0 issues every TMA copy
+//   warp  10    lane 0 issues tile L's MMAs and commits
+//   warp  11    idle
 // Registers: launched at 168 per thread; the control warpgroup drops to 56
-// and the two softmax warpgroups rise to 224 (2*128*224 + 128*56 = 384*168),
-// enough to keep a whole 128-column score row in registers.
+// and the two softmax warpgroups rise to 224 (2*128*224 + 128*56 = 384*168).
 //
-// MMA issue order (M4.6 0x08 startup / steady / drain):
-//   QK_H(0) QK_L(0) | PV_H(j-1) QK_H(j) PV_L(j-1) QK_L(j) ... | PV_H PV_L
-// P_X(j-1) lives in the columns QK_X(j) overwrites; as in the pages' FA4
-// schedule, PV_X(j-1) is issued by the same thread before QK_X(j).
+// Per tile X and key tile j (M4.6 0x08-0x09 roles, own protocol):
+//   MMA X:     QK_X(0); then for j: [S_X(j) copied] QK_X(j+1);
+//              [P_X(j) written] PV_X(j) -> commit p_free_X
+//   softmax X: [S_X(j) ready] load S -> signal S free -> row max ->
+//              [PV_X(j-1) done] rescale O if needed, write P_X(j) -> signal
+// K/V slots are loaded in the order the MMAs need them:
+//   K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.
 //
 // Online softmax (M4.3 0x07-0x09; M4.6 0x09 conditional rescaling): each
 // softmax thread keeps its row's retained reference r (raw score units) and
@@ -55,8 +66,9 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxRegs = 224;
 constexpr int kControlRegs = 56;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * 168, "register split");
-constexpr int kMmaWarp = 8;
+constexpr int kMmaWarpH = 8;
 constexpr int kLoadWarp = 9;
+constexpr int kMmaWarpL = 10;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units (fp16/bf16 row of M4.6 0x09 table)
 
 template <int D>
@@ -64,9 +76,11 @@ struct Cfg {
   static constexpr int kColBlocks = D / 64;           // 128-byte swizzle column blocks
   static constexpr int kTileBytes = kBM * D * 2;      // one 128 x D 16-bit tile
   static constexpr int kBlockBytes = kBM * 128;       // one 128-row x 128-byte block
-  static constexpr int kStages = (D == 128) ? 4 : 6;  // K/V ring slots
+  static constexpr int kPBytes = kBM * kBN * 2;       // one 128 x 128 16-bit P tile
+  static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring slots
   static constexpr int kQOff = 0;
-  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kPOff = 2 * kTileBytes;
+  static constexpr int kRingOff = kPOff + 2 * kPBytes;
   static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
   static constexpr int kSmemBytes = 1024 + kBarOff + 512;  // + alignment slack + barriers
 };
@@ -88,9 +102,11 @@ struct __align__(8) Barriers {
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t s_full[2];
+  uint64_t s_free[2];
   uint64_t p_full[2];
+  uint64_t p_free[2];
   uint64_t o_full[2];
-  uint64_t mma_done;
+  uint64_t mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -110,6 +126,11 @@ __device__ __forceinline__ int tiles_for(int q0, int Sq, int Sk, int causal, int
   return min(nk, lim / kBN + 1);
 }
 
+// Position of K_j / V_j in the load order K_0, K_1, V_0, K_2, V_1, ...,
+// K_{n-1}, V_{n-2}, V_{n-1} (n key tiles).
+__device__ __forceinline__ int item_of_k(int j) { return j == 0 ? 0 : 2 * j - 1; }
+__device__ __forceinline__ int item_of_v(int j, int n) { return j <= n - 2 ? 2 * j + 2 : 2 * n - 1; }
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -120,6 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + C::kQOff;
+  uint8_t* sP = smem + C::kPOff;
   uint8_t* sRing = smem + C::kRingOff;
   Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kBarOff);
   volatile int* abort_flag = &bars->abort_flag;
@@ -152,14 +174,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
-      mbar_init(&bars->kv_empty[s], 1);
+      mbar_init(&bars->kv_empty[s], 2);  // released by both MMA issuers
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
+      mbar_init(&bars->s_free[x], kBM);
       mbar_init(&bars->p_full[x], kBM);
+      mbar_init(&bars->p_free[x], 1);
       mbar_init(&bars->o_full[x], 1);
+      mbar_init(&bars->mma_done[x], 1);
     }
-    mbar_init(&bars->mma_done, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -168,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarpH) {
     tmem_alloc(&bars->tmem_base, 512);
     tmem_relinquish();
   }
@@ -178,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp >= 8) {
-    // ---- control warpgroup: TMA loader and MMA issuer
+    // ---- control warpgroup: TMA loader and MMA issuers
     regs_dec<kControlRegs>();
     if (warp == kLoadWarp) {
       // ================================================================ loader
@@ -202,12 +226,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ph = (it / C::kStages) & 1;
           if (!bounded_wait(&bars->kv_empty[st], ph ^ 1, abort_flag, p.status, kStatusTimeoutLoad))
             break;
-          const CUtensorMap* map = (it & 1) ? &tmap_v : &tmap_k;
-          const int key0 = (it >> 1) * kBN;
+          // item -> (K or V, key tile) in the order K_0, K_1, V_0, K_2, V_1, ...
+          bool is_v;
+          int jt;
+          if (it == 0) {
+            is_v = false, jt = 0;
+          } else if (it & 1) {
+            if (it == n_items - 1) is_v = true, jt = n_max - 1;
+            else is_v = false, jt = (it + 1) / 2;
+          } else {
+            is_v = true, jt = (it - 2) / 2;
+          }
           mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
           for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(sRing + st * C::kTileBytes + cb * C::kBlockBytes, map, &bars->kv_full[st],
-                        cb * 64, key0, b * p.Hkv + kvh, keep);
+            tma_load_3d(sRing + st * C::kTileBytes + cb * C::kBlockBytes, is_v ? &tmap_v : &tmap_k,
+                        &bars->kv_full[st], cb * 64, jt * kBN, b * p.Hkv + kvh, keep);
           issued = it + 1;
         }
         // Drain: every copy this thread issued must have landed before exit.
@@ -222,72 +255,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // ================================================================ MMA issuer
-      // One thread issues both tiles' MMAs, which keeps the two tiles
-      // alternating on the tensor pipe (H's softmax overlaps L's MMAs and
-      // vice versa).  Step j waits for K_j and V_{j-1} first (normally landed
-      // long before), then for each tile's P, so PV and QK issue back to back.
+    } else if (warp == kMmaWarpH || warp == kMmaWarpL) {
+      // ================================================================ MMA issuers
+      // One issuing thread per query tile.  Both release every K/V slot (the
+      // empty barriers count two arrivals); key tiles a query tile does not
+      // visit (causal: H needs one fewer than L) are released once landed.
       if (lane == 0) {
+        const int x = (warp == kMmaWarpH) ? 0 : 1;
+        const int nt = x ? nt_l : nt_h;
         constexpr uint32_t kIdescQK = idesc_f16(BF16, false, false, kBM, kBN);
         constexpr uint32_t kIdescPV = idesc_f16(BF16, false, true, kBM, D);
         const uint32_t ring_addr = smem_u32(sRing);
+        const uint32_t s_col = tmem + x * kBN;
+        const uint32_t o_col = tmem + 2 * kBN + x * D;
         // Descriptors are built once; a K-step only adds (byte offset >> 4)
         // to the start-address field (every offset stays inside its tile).
-        const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
-        auto issue_qk = [&](int x, int st) {
-          const uint64_t qd = q_desc + ((x * C::kTileBytes) >> 4);
+        const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ + x * C::kTileBytes), 16, 1024);
+        const uint64_t p_desc = smem_desc_sw128(smem_u32(sP + x * C::kPBytes), 16, 1024);
+        auto slot_of = [&](int item, uint32_t& parity) {
+          parity = (item / C::kStages) & 1;
+          return item % C::kStages;
+        };
+        auto issue_qk = [&](int st) {
           const uint64_t kd = smem_desc_sw128(ring_addr + st * C::kTileBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint64_t off = ((kk / 4) * C::kBlockBytes + (kk % 4) * 32) >> 4;
-            mma_f16_ss(tmem + x * kBN, qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
+            mma_f16_ss(s_col, q_desc + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
         };
-        auto issue_pv = [&](int x, int st, bool accumulate) {
+        auto issue_pv = [&](int st, bool accumulate) {
           const uint64_t vd = smem_desc_sw128(ring_addr + st * C::kTileBytes, C::kBlockBytes, 1024);
-          const uint32_t s_col = tmem + x * kBN;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_f16_ts(tmem + 2 * kBN + x * D, s_col + kBN / 2 + kk * 8, vd + ((kk * 2048) >> 4),
-                       kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
-        };
-        bool ok = n_max == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
-        // Step j issues PV_X(j-1) then QK_X(j) for X = H, L; step n_max drains.
-        for (int j = 0; ok && j <= n_max; ++j) {
-          const bool have_v = j > 0, have_k = j < n_max;
-          const int itK = 2 * j, itV = 2 * j - 1;
-          const int stK = itK % C::kStages, stV = have_v ? itV % C::kStages : 0;
-          if (have_k && !(ok = bounded_wait(&bars->kv_full[stK], (itK / C::kStages) & 1, abort_flag,
-                                            p.status, kStatusTimeoutMma)))
-            break;
-          if (have_v && !(ok = bounded_wait(&bars->kv_full[stV], (itV / C::kStages) & 1, abort_flag,
-                                            p.status, kStatusTimeoutMma)))
-            break;
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            const int nt = x ? nt_l : nt_h;
-            if (have_v && j - 1 < nt) {
-              if (!(ok = bounded_wait(&bars->p_full[x], (j - 1) & 1, abort_flag, p.status,
-                                      kStatusTimeoutMma)))
-                break;
-              tc_fence_after();
-              issue_pv(x, stV, j - 1 > 0);
-              if (j - 1 == nt - 1) mma_commit(&bars->o_full[x]);
-            }
-            if (have_k && j < nt) {
-              issue_qk(x, stK);
-              mma_commit(&bars->s_full[x]);
-            }
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t poff = ((kk / 4) * C::kBlockBytes + (kk % 4) * 32) >> 4;
+            mma_f16_ss(o_col, p_desc + poff, vd + ((kk * 2048) >> 4), kIdescPV,
+                       (accumulate || kk > 0) ? 1u : 0u);
           }
-          if (!ok) break;
-          if (have_v) mma_commit(&bars->kv_empty[stV]);
-          if (have_k) mma_commit(&bars->kv_empty[stK]);
+        };
+        bool ok = nt == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
+        // S_X(0)
+        if (ok && nt > 0) {
+          uint32_t par;
+          const int st = slot_of(item_of_k(0), par);
+          ok = bounded_wait(&bars->kv_full[st], par, abort_flag, p.status, kStatusTimeoutMma);
+          if (ok) {
+            issue_qk(st);
+            mma_commit(&bars->s_full[x]);
+            mma_commit(&bars->kv_empty[st]);
+          }
+        }
+        for (int j = 0; ok && j < nt; ++j) {
+          // QK_X(j+1) once the softmax threads hold S_X(j) in registers
+          if (j + 1 < nt) {
+            uint32_t par;
+            const int st = slot_of(item_of_k(j + 1), par);
+            if (!(ok = bounded_wait(&bars->kv_full[st], par, abort_flag, p.status, kStatusTimeoutMma)))
+              break;
+            if (!(ok = bounded_wait(&bars->s_free[x], j & 1, abort_flag, p.status, kStatusTimeoutMma)))
+              break;
+            tc_fence_after();
+            issue_qk(st);
+            mma_commit(&bars->s_full[x]);
+            mma_commit(&bars->kv_empty[st]);
+          }
+          // PV_X(j) once P_X(j) is in shared memory (and O_X corrected)
+          {
+            uint32_t par;
+            const int st = slot_of(item_of_v(j, n_max), par);
+            if (!(ok = bounded_wait(&bars->kv_full[st], par, abort_flag, p.status, kStatusTimeoutMma)))
+              break;
+            if (!(ok = bounded_wait(&bars->p_full[x], j & 1, abort_flag, p.status, kStatusTimeoutMma)))
+              break;
+            tc_fence_after();
+            issue_pv(st, j > 0);
+            mma_commit(&bars->p_free[x]);
+            if (j == nt - 1) mma_commit(&bars->o_full[x]);
+            mma_commit(&bars->kv_empty[st]);
+          }
+        }
+        // Release the K/V slots of key tiles this query tile does not visit.
+        for (int j = nt; ok && j < n_max; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            uint32_t par;
+            const int st = slot_of(kv ? item_of_v(j, n_max) : item_of_k(j), par);
+            if (!(ok = bounded_wait(&bars->kv_full[st], par, abort_flag, p.status, kStatusTimeoutMma)))
+              break;
+            mbar_arrive(&bars->kv_empty[st]);
+          }
         }
         // Every MMA this thread issued must complete before TMEM is released.
-        mma_commit(&bars->mma_done);
+        mma_commit(&bars->mma_done[x]);
         int dummy = 0;
-        bounded_wait(&bars->mma_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status,
+        bounded_wait(&bars->mma_done[x], 0, reinterpret_cast<volatile int*>(&dummy), p.status,
                      kStatusTimeoutDrain);
       }
       __syncwarp();
@@ -304,6 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + x * kBN;
     const uint32_t o_tmem = tmem + lane_off + 2 * kBN + x * D;
+    // This row of P_X in shared memory: two 64-key column blocks of 128-byte
+    // rows; 16-byte chunk c of the row sits at chunk c ^ (row % 8).
+    uint8_t* p_row = sP + x * C::kPBytes + row * 128;
     const float lam = p.scale_log2;
     float r = -INFINITY;  // retained reference, raw score units
     float l = 0.f;
@@ -317,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // ---- S row -> registers (four loads in flight, one wait)
+      // ---- S row -> registers (four loads in flight, one wait), then S_X is free
       uint32_t u[kBN];
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c)
@@ -325,6 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+      tc_fence_before();
+      mbar_arrive(&bars->s_free[x]);
       float* s = reinterpret_cast<float*>(u);
       const int k0 = j * kBN;
       const bool tail = k0 + kBN > p.Sk;
@@ -357,44 +422,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       l *= gamma;
-      // ---- P = 2^(lambda*s - lambda*r), row sum, pack to 16 bits, store to TMEM
+      // ---- P_X(j-1) has been consumed (and O_X is stable) once PV_X(j-1) is done
+      if (j > 0) {
+        ok = bounded_wait(&bars->p_free[x], (j - 1) & 1, abort_flag, p.status, kStatusTimeoutSoftmax);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // correction: O_row *= gamma (warp-uniform path; gamma = 1 rows unchanged)
+        if (__any_sync(0xffffffffu, gamma != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t w32[32];
+            tmem_ld32(o_tmem + c * 32, w32);
+            tmem_wait_ld();
+            reg_fence32(w32);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) w32[i] = __float_as_uint(__uint_as_float(w32[i]) * gamma);
+            tmem_st32(o_tmem + c * 32, w32);
+          }
+          tmem_wait_st();
+        }
+      }
+      // ---- P = 2^(lambda*s - lambda*r), row sum, pack to 16 bits, store the
+      // row of P_X(j) into shared memory (swizzled K-major A operand)
       const float rs = (r == -INFINITY) ? 0.f : r * lam;
       const float2 lam2 = make_float2(lam, lam);
       const float2 nrs2 = make_float2(-rs, -rs);
       float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int ch = 0; ch < kBN / 8; ++ch) {  // 16-byte chunks of 8 keys
+        uint32_t pk[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = half * 64 + 2 * i;
+        for (int i = 0; i < 4; ++i) {
+          const int c = ch * 8 + 2 * i;
           float2 t = ffma2(make_float2(s[c], s[c + 1]), lam2, nrs2);
           t.x = ex2_approx(t.x);
           t.y = ex2_approx(t.y);
-          sum4[i & 3] = fadd2(sum4[i & 3], t);
+          sum4[i] = fadd2(sum4[i], t);
           pk[i] = pack2<BF16>(t.x, t.y);
         }
-        tmem_st32(s_tmem + kBN / 2 + half * 32, pk);
+        const int blk = ch / 8, c8 = ch % 8;
+        *reinterpret_cast<uint4*>(p_row + blk * C::kBlockBytes + ((c8 ^ (row & 7)) << 4)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
       const float2 s01 = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
       l += s01.x + s01.y;
-      // ---- correction: O_row *= gamma once the scores are dead (warp-uniform
-      // path; rows whose reference did not move carry gamma = 1)
-      if (j > 0 && __any_sync(0xffffffffu, gamma != 1.f)) {
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t w32[32];
-          tmem_ld32(o_tmem + c * 32, w32);
-          tmem_wait_ld();
-          reg_fence32(w32);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w32[i] = __float_as_uint(__uint_as_float(w32[i]) * gamma);
-          tmem_st32(o_tmem + c * 32, w32);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
+      fence_proxy_async_smem();  // P stores -> visible to the tensor core (async proxy)
+      tc_fence_before();         // O correction (tcgen05.st) ordered before the arrive
       mbar_arrive(&bars->p_full[x]);
     }
 
@@ -442,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarpH) tmem_dealloc(tmem, 512);
 }
 
 template <int D, bool BF16, bool CAUSAL>
