@@ -17,4 +17,6 @@ from .oracle import (  # noqa: F401
     decode_chunk_states,
     decode_chunk_bounds,
     num_threads,
+    attn_bwd,
+    attn_bwd_kvheads,
 )

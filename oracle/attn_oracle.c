@@ -23,6 +23,11 @@
  *   M4.4 0x05.1A / 0x05.1F (causal):
  *       visible(q, k) iff k <= q + delta, delta = S_k - S_q (bottom-right)
  *
+ * The backward pass (oracle_attn_bwd, below) is the gradient of that
+ * definition as M4.4 0x06.1A writes it: dP = dO V^T, dS = P o (dP - rowsum(P o dP)),
+ * dQ = tau dS K, dK = tau dS^T Q, dV = P^T dO, summed over query-head groups
+ * for GQA (0x06.1H).
+ *
  * Policies where the pages leave a choice open (each is a stated reading):
  *   - causal alignment is bottom-right, delta = S_k - S_q (M4.4 0x05.1F);
  *   - a row with no visible key (only possible when causal and S_q > S_k)
@@ -255,6 +260,184 @@ int oracle_decode_chunk_states(const float *q, const float *k, const float *v,
         l_out[s] = l;
     }
     return ORACLE_OK;
+}
+
+/*
+ * Exact attention backward, M4.4 "FlashAttention-2 Work Partitioning and the
+ * Decode Boundary", 0x06.1A: with S = tau Q K^T (masked before the row
+ * normalisation), P = softmax_row(S), O = P V and the incoming gradient dO,
+ *
+ *     dP    = dO V^T
+ *     dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)     (row softmax Jacobian
+ *                                                  contracted with dP)
+ *     dQ    = tau dS K,   dK = tau dS^T Q,   dV = P^T dO
+ *
+ * and, for grouped-query heads (0x06.1H), the K/V gradient of a KV head is
+ * the sum over the g query heads that read it.  Invisible (masked) entries
+ * have P = 0 and contribute nothing; a row with no visible key has
+ * dQ = 0 and contributes nothing.
+ *
+ * The row scalar is computed here from its definition, sum_k P_ik dP_ik,
+ * not from the saved-output shortcut dO_i . O_i that the pages derive from
+ * it (the tests check that identity against this oracle).
+ *
+ * Organisation for one (b, kv_head) pair (no tiling, no streaming):
+ *   pass 1, one query row at a time (h in the group, i): materialise the
+ *           visible scores, P_i, dP_i, the row scalar D_i and dQ_i; keep
+ *           LSE_i = m + log l and D_i;
+ *   pass 2, one key row at a time: dK_j and dV_j as sums over the query
+ *           rows that see key j, with P_ij = exp(S_ij - LSE_i) (the same
+ *           softmax written through the row's log-normaliser).
+ * The split only gives every output element a single writer.
+ */
+static void bwd_group(const float *q, const float *k, const float *v, const float *dout,
+                      int b, int kvh, int H, int Hkv, int Sq, int Sk, int d, double scale,
+                      int causal, double *dq /* [g, Sq, d] */, double *dk /* [Sk, d] */,
+                      double *dv /* [Sk, d] */, double *lse_row /* [g * Sq] */,
+                      double *D_row /* [g * Sq] */, int *bad)
+{
+    const int g = H / Hkv;
+    const long long n_rows = (long long)g * Sq;
+    const float *kb = k + ((long long)b * Hkv + kvh) * (long long)Sk * d;
+    const float *vb = v + ((long long)b * Hkv + kvh) * (long long)Sk * d;
+    /* query head h = kvh * g + hh of batch b */
+#define QROW(hh, i) (q + (((long long)b * H + (long long)kvh * g + (hh)) * Sq + (i)) * (long long)d)
+#define DOROW(hh, i) (dout + (((long long)b * H + (long long)kvh * g + (hh)) * Sq + (i)) * (long long)d)
+
+    /* pass 1: per query row */
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)Sk);
+        double *dp = (double *)malloc(sizeof(double) * (size_t)Sk);
+        if (!s || !dp) {
+#pragma omp atomic write
+            *bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (long long r = 0; r < n_rows; ++r) {
+                const int hh = (int)(r / Sq), i = (int)(r % Sq);
+                const float *qi = QROW(hh, i), *doi = DOROW(hh, i);
+                double *dqi = dq + r * (long long)d;
+                const long long n_vis = visible_prefix(i, Sq, Sk, causal);
+                for (int t = 0; t < d; ++t) dqi[t] = 0.0;
+                if (n_vis <= 0) {
+                    lse_row[r] = -INFINITY;
+                    D_row[r] = 0.0;
+                    continue;
+                }
+                double m = -INFINITY;
+                for (long long j = 0; j < n_vis; ++j) {
+                    double dot = 0.0, dpj = 0.0;
+                    for (int t = 0; t < d; ++t) {
+                        dot += (double)qi[t] * (double)kb[j * d + t];
+                        dpj += (double)doi[t] * (double)vb[j * d + t];
+                    }
+                    s[j] = scale * dot;
+                    dp[j] = dpj;
+                    if (s[j] > m) m = s[j];
+                }
+                double l = 0.0;
+                for (long long j = 0; j < n_vis; ++j) l += exp(s[j] - m);
+                double Di = 0.0;
+                for (long long j = 0; j < n_vis; ++j) {
+                    s[j] = exp(s[j] - m) / l; /* s now holds P_ij */
+                    Di += s[j] * dp[j];
+                }
+                for (long long j = 0; j < n_vis; ++j) {
+                    const double dsij = s[j] * (dp[j] - Di);
+                    for (int t = 0; t < d; ++t) dqi[t] += scale * dsij * (double)kb[j * d + t];
+                }
+                lse_row[r] = m + log(l);
+                D_row[r] = Di;
+            }
+        }
+        free(s);
+        free(dp);
+    }
+    if (*bad) return;
+
+    /* pass 2: per key row */
+#pragma omp parallel for schedule(dynamic, 4)
+    for (long long j = 0; j < Sk; ++j) {
+        double *dkj = dk + j * (long long)d, *dvj = dv + j * (long long)d;
+        for (int t = 0; t < d; ++t) dkj[t] = dvj[t] = 0.0;
+        for (long long r = 0; r < n_rows; ++r) {
+            const int hh = (int)(r / Sq), i = (int)(r % Sq);
+            if (j >= visible_prefix(i, Sq, Sk, causal)) continue;
+            const float *qi = QROW(hh, i), *doi = DOROW(hh, i);
+            double dot = 0.0, dpj = 0.0;
+            for (int t = 0; t < d; ++t) {
+                dot += (double)qi[t] * (double)kb[j * d + t];
+                dpj += (double)doi[t] * (double)vb[j * d + t];
+            }
+            const double pij = exp(scale * dot - lse_row[r]);
+            const double dsij = pij * (dpj - D_row[r]);
+            for (int t = 0; t < d; ++t) {
+                dkj[t] += scale * dsij * (double)qi[t];
+                dvj[t] += pij * (double)doi[t];
+            }
+        }
+    }
+#undef QROW
+#undef DOROW
+}
+
+/*
+ * Backward for every head: dq [B,H,Sq,d], dk/dv [B,Hkv,Sk,d], and (if not
+ * NULL) the row scalars D [B,H,Sq] and LSE [B,H,Sq].
+ */
+int oracle_attn_bwd(const float *q, const float *k, const float *v, const float *dout,
+                    int B, int H, int Hkv, int Sq, int Sk, int d, double scale, int causal,
+                    double *dq, double *dk, double *dv, double *D_out, double *lse_out)
+{
+    if (B < 1 || Sq < 1 || Sk < 1 || d < 1 || check_heads(H, Hkv)) return ORACLE_EARG;
+    const int g = H / Hkv;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)g * Sq);
+    double *D = (double *)malloc(sizeof(double) * (size_t)g * Sq);
+    int bad = (!lse || !D);
+    for (int b = 0; b < B && !bad; ++b)
+        for (int kvh = 0; kvh < Hkv && !bad; ++kvh) {
+            const long long h0 = (long long)b * H + (long long)kvh * g; /* first query head */
+            bwd_group(q, k, v, dout, b, kvh, H, Hkv, Sq, Sk, d, scale, causal,
+                      dq + h0 * Sq * (long long)d,
+                      dk + ((long long)b * Hkv + kvh) * (long long)Sk * d,
+                      dv + ((long long)b * Hkv + kvh) * (long long)Sk * d, lse, D, &bad);
+            for (long long r = 0; r < (long long)g * Sq; ++r) {
+                if (D_out) D_out[h0 * Sq + r] = D[r];
+                if (lse_out) lse_out[h0 * Sq + r] = lse[r];
+            }
+        }
+    free(lse);
+    free(D);
+    return bad ? ORACLE_EARG : ORACLE_OK;
+}
+
+/*
+ * Backward restricted to chosen KV heads (for sampled checks of large
+ * problems): kv_ids[n] = b * Hkv + kv_head.  For each chosen pair it returns
+ * dq of its g query heads [n, g, Sq, d] and its dk, dv [n, Sk, d].
+ */
+int oracle_attn_bwd_kvheads(const float *q, const float *k, const float *v, const float *dout,
+                            int B, int H, int Hkv, int Sq, int Sk, int d, double scale,
+                            int causal, const long long *kv_ids, long long n,
+                            double *dq, double *dk, double *dv)
+{
+    if (B < 1 || Sq < 1 || Sk < 1 || d < 1 || check_heads(H, Hkv)) return ORACLE_EARG;
+    for (long long r = 0; r < n; ++r)
+        if (kv_ids[r] < 0 || kv_ids[r] >= (long long)B * Hkv) return ORACLE_EARG;
+    const int g = H / Hkv;
+    double *lse = (double *)malloc(sizeof(double) * (size_t)g * Sq);
+    double *D = (double *)malloc(sizeof(double) * (size_t)g * Sq);
+    int bad = (!lse || !D);
+    for (long long r = 0; r < n && !bad; ++r) {
+        const int b = (int)(kv_ids[r] / Hkv), kvh = (int)(kv_ids[r] % Hkv);
+        bwd_group(q, k, v, dout, b, kvh, H, Hkv, Sq, Sk, d, scale, causal,
+                  dq + r * (long long)g * Sq * d, dk + r * (long long)Sk * d,
+                  dv + r * (long long)Sk * d, lse, D, &bad);
+    }
+    free(lse);
+    free(D);
+    return bad ? ORACLE_EARG : ORACLE_OK;
 }
 
 /* Number of threads the oracle's parallel regions use (for reporting). */

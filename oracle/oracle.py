@@ -53,9 +53,14 @@ def _load():
                                                     i64p, cll, f64p, f64p]
             lib.oracle_decode_chunk_states.argtypes = [f32p, f32p, f32p, i32p, ci, ci, ci, ci, ci,
                                                        cd, ci, f64p, f64p, f64p, i64p]
+            lib.oracle_attn_bwd.argtypes = [f32p, f32p, f32p, f32p, ci, ci, ci, ci, ci, ci, cd, ci,
+                                            f64p, f64p, f64p, f64p, f64p]
+            lib.oracle_attn_bwd_kvheads.argtypes = [f32p, f32p, f32p, f32p, ci, ci, ci, ci, ci, ci, cd,
+                                                    ci, i64p, cll, f64p, f64p, f64p]
             lib.oracle_num_threads.argtypes = []
             for fn in (lib.oracle_attn_fwd_rows, lib.oracle_attn_fwd, lib.oracle_attn_decode_rows,
-                       lib.oracle_decode_chunk_states, lib.oracle_num_threads):
+                       lib.oracle_decode_chunk_states, lib.oracle_attn_bwd, lib.oracle_attn_bwd_kvheads,
+                       lib.oracle_num_threads):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -160,3 +165,52 @@ def decode_chunk_states(q, k, v, seqlens, scale: float, n_split: int):
     if rc != 0:
         raise ValueError(f"oracle_decode_chunk_states rejected its arguments (rc={rc})")
     return m, l, u, cnt
+
+
+def attn_bwd(q, k, v, dout, scale: float, causal: bool):
+    """Exact backward from the definition (M4.4 0x06.1A), fp64.
+
+    q, dout [B,H,Sq,d]; k, v [B,Hkv,Sk,d].  Returns dq [B,H,Sq,d],
+    dk, dv [B,Hkv,Sk,d] (summed over each KV head's query-head group),
+    the row scalars D = sum_j P_ij dP_ij [B,H,Sq] and LSE [B,H,Sq]."""
+    B, H, Sq, d = q.shape
+    _, Hkv, Sk, _ = k.shape
+    q, qp = _f32(q)
+    k, kp = _f32(k)
+    v, vp = _f32(v)
+    do, dop = _f32(dout)
+    dq = np.empty((B, H, Sq, d), dtype=np.float64)
+    dk = np.empty((B, Hkv, Sk, d), dtype=np.float64)
+    dv = np.empty((B, Hkv, Sk, d), dtype=np.float64)
+    D = np.empty((B, H, Sq), dtype=np.float64)
+    lse = np.empty((B, H, Sq), dtype=np.float64)
+    c = ctypes.c_double
+    rc = _load().oracle_attn_bwd(qp, kp, vp, dop, B, H, Hkv, Sq, Sk, d, float(scale), int(bool(causal)),
+                                 _ptr(dq, c), _ptr(dk, c), _ptr(dv, c), _ptr(D, c), _ptr(lse, c))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd rejected its arguments (rc={rc})")
+    return dq, dk, dv, D, lse
+
+
+def attn_bwd_kvheads(q, k, v, dout, scale: float, causal: bool, kv_ids):
+    """Backward restricted to chosen KV heads, kv id = b*Hkv + kv_head.
+    Returns dq [n, g, Sq, d] (the group's query heads), dk, dv [n, Sk, d]."""
+    B, H, Sq, d = q.shape
+    _, Hkv, Sk, _ = k.shape
+    g = H // Hkv
+    q, qp = _f32(q)
+    k, kp = _f32(k)
+    v, vp = _f32(v)
+    do, dop = _f32(dout)
+    ids = np.ascontiguousarray(kv_ids, dtype=np.int64)
+    n = len(ids)
+    dq = np.empty((n, g, Sq, d), dtype=np.float64)
+    dk = np.empty((n, Sk, d), dtype=np.float64)
+    dv = np.empty((n, Sk, d), dtype=np.float64)
+    c = ctypes.c_double
+    rc = _load().oracle_attn_bwd_kvheads(qp, kp, vp, dop, B, H, Hkv, Sq, Sk, d, float(scale),
+                                         int(bool(causal)), _ptr(ids, ctypes.c_longlong), n,
+                                         _ptr(dq, c), _ptr(dk, c), _ptr(dv, c))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd_kvheads rejected its arguments (rc={rc})")
+    return dq, dk, dv
