@@ -1,7 +1,7 @@
 """exact_tiled_attention_gb300 -- exact tiled attention for GB300 (sm_103a).
 
 The computation lives in libgbattn.so (hand-written CUDA: TMA + tcgen05 +
-TMEM prefill forward, split-KV decode with a merge kernel) behind the C ABI in
+TMEM prefill forward and backward, split-KV decode with a merge kernel) behind the C ABI in
 include/gbattn.h.  This package is its Python binding; it loads the library on
 first use and raises if it is missing (there is no fallback path).
 """
@@ -9,7 +9,10 @@ from .binding import (  # noqa: F401
     EXPORTS,
     GbattnError,
     LIB_PATH,
+    attn_bwd,
+    attn_bwd_workspace_bytes,
     attn_decode_splitkv,
+    attn_decode_splitkv_noalloc,
     attn_decode_workspace_bytes,
     attn_fwd,
     error_string,

@@ -27,6 +27,8 @@ ERRORS = {
     -8: "GBATTN_EDEVICE_TIMEOUT", -9: "GBATTN_ESPLIT", -10: "GBATTN_EUNSUPPORTED",
 }
 EXPORTS = ("attn_fwd", "attn_decode_workspace_bytes", "attn_decode_splitkv",
+           "attn_decode_splitkv_noalloc", "attn_decode_noalloc_scratch_bytes",
+           "attn_bwd_workspace_bytes", "attn_bwd",
            "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_error_string",
            "gbattn_version")
 
@@ -65,6 +67,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_decode_splitkv_noalloc.restype = ci
         lib.attn_decode_noalloc_scratch_bytes.argtypes = []
         lib.attn_decode_noalloc_scratch_bytes.restype = sz
+        lib.attn_bwd_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.attn_bwd_workspace_bytes.restype = sz
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
+                                 sz, ci, vp]
+        lib.attn_bwd.restype = ci
         lib.gbattn_causal_tile_counts.argtypes = [ci, ci, ci, ci, ll_p, ll_p, ll_p, ll_p, ll_p]
         lib.gbattn_causal_tile_counts.restype = ci
         lib.gbattn_device_status.argtypes = []
@@ -213,6 +220,49 @@ def attn_decode_splitkv_noalloc(q, k_cache, v_cache, seqlens, scale: float | Non
     if rc != GBATTN_OK:
         raise GbattnError(rc, "attn_decode_splitkv_noalloc")
     return out, lse
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, Sq: int, d: int) -> int:
+    return int(load_library().attn_bwd_workspace_bytes(B, H, Sq, d))
+
+
+def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
+             workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Exact attention backward through the C ABI `attn_bwd`.
+
+    q, o, dout [B,H,Sq,d]; k, v [B,Hkv,Sk,d] (fp16/bf16, CUDA, contiguous);
+    lse [B,H,Sq] fp32 from attn_fwd.  workspace: optional caller-owned CUDA
+    buffer of at least attn_bwd_workspace_bytes(B, H, Sq, d) bytes (allocated
+    here if omitted).  Returns (dq, dk, dv)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check(t, n, 4)
+    B, H, Sq, d = q.shape
+    Bk, Hkv, Sk, dk_ = k.shape
+    if k.shape != v.shape or Bk != B or dk_ != d or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shape mismatch between q, k, v, o and dout")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise TypeError("q, k, v, o, dout must share one dtype")
+    if not isinstance(lse, torch.Tensor) or not lse.is_cuda or lse.dtype != torch.float32 or \
+            tuple(lse.shape) != (B, H, Sq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 CUDA tensor [B, H, Sq]")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lib = load_library()
+    need = int(lib.attn_bwd_workspace_bytes(B, H, Sq, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, Sq, Sk,
+                      d, float(scale), int(bool(causal)), workspace.data_ptr(), ws_bytes, dt,
+                      _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def gbattn_causal_tile_counts(Sq: int, Sk: int, Br: int, Bc: int) -> dict:

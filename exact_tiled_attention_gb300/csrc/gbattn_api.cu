@@ -178,6 +178,60 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   return launch_decode(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
+static size_t bwd_d_bytes(int B, int H, int Sq) {
+  // row scalars D, rounded up to 256 bytes so the accumulator stays aligned
+  return ((static_cast<size_t>(B) * H * Sq * sizeof(float)) + 255) & ~static_cast<size_t>(255);
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int Sq, int d) {
+  if (B < 1 || H < 1 || Sq < 1 || d < 1) return 0;
+  return bwd_d_bytes(B, H, Sq) + static_cast<size_t>(B) * H * Sq * d * sizeof(float);
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Sq, int Sk,
+             int d, float scale, int causal, void* workspace, size_t workspace_bytes, int dtype,
+             void* stream) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return GBATTN_EBADSHAPE;
+  if (H % Hkv != 0) return GBATTN_EHEADS;
+  if (d != 128) return GBATTN_EHEADDIM;
+  if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
+  const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return GBATTN_EPOINTER;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return GBATTN_EPOINTER;
+  if (static_cast<long long>(B) * H > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
+    return GBATTN_EBADSHAPE;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, Sq, d)) return GBATTN_EWORKSPACE;
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  BackwardArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.Dvec = static_cast<float*>(workspace);
+  a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + bwd_d_bytes(B, H, Sq));
+  a.bf16 = dtype == GBATTN_BF16;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status;
+  return launch_backward(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
 int gbattn_causal_tile_counts(int Sq, int Sk, int Br, int Bc, long long* full, long long* partial,
                               long long* skipped, long long* allowed_cells,
                               long long* visited_cells) {
@@ -241,10 +295,10 @@ const char* gbattn_error_string(int code) {
     case GBATTN_OK: return "ok";
     case GBATTN_EBADSHAPE: return "bad shape (a size is < 1 or too large)";
     case GBATTN_EHEADS: return "query heads are not a multiple of KV heads";
-    case GBATTN_EHEADDIM: return "unsupported head dimension (only 64 and 128)";
+    case GBATTN_EHEADDIM: return "unsupported head dimension (64 and 128; backward: 128)";
     case GBATTN_EDTYPE: return "unsupported dtype (only fp16 and bf16)";
     case GBATTN_EPOINTER: return "null or misaligned pointer";
-    case GBATTN_EWORKSPACE: return "decode workspace too small";
+    case GBATTN_EWORKSPACE: return "workspace too small (or problem beyond a fixed scratch size)";
     case GBATTN_ELAUNCH: return "CUDA launch or tensor-map encoding failed";
     case GBATTN_EDEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
     case GBATTN_ESPLIT: return "n_split out of range (1..256)";

@@ -41,10 +41,32 @@ struct DecodeArgs {
   int* status;
 };
 
+// Arguments of one backward (preprocess + main + dQ conversion).
+struct BackwardArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, H, Hkv, Sq, Sk, d;
+  float scale;
+  int causal;
+  float* Dvec;    // workspace: [B*H*Sq] fp32
+  float* dq_acc;  // workspace: [B*H*Sq*d] fp32
+  bool bf16;
+  cudaStream_t stream;
+  int* status;
+};
+
 // Each returns a cudaError_t / CUresult folded into 0 (ok) or -1 (launch or
 // tensor-map failure).
 int launch_prefill(const PrefillArgs& a);
 int launch_decode(const DecodeArgs& a);
+int launch_backward(const BackwardArgs& a);
 
 // cuTensorMapEncodeTiled fetched once through the runtime's driver entry
 // point (no link-time dependency on libcuda).

@@ -20,6 +20,7 @@ enum DeviceStatus : int {
   kStatusTimeoutSoftmax = 3,  // softmax waited too long for S or O
   kStatusTimeoutDrain = 4,    // teardown wait for in-flight copies or MMAs
   kStatusTimeoutDecode = 5,   // decode consumer/producer wait
+  kStatusTimeoutBwd = 6,      // backward kernel wait (any role)
 };
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.
@@ -119,6 +120,47 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// Bulk (non-tensor) asynchronous reduction: global[dst .. dst+bytes) +=
+// shared[src .. src+bytes) element-wise in fp32.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.  Tracked by the issuing thread's bulk
+// async-group (commit / wait below).
+__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until every committed bulk group of this thread has finished READING
+// its shared-memory source (the source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_group_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32) that also returns
+// the AND of `pred` over them; every participating thread must arrive.
+__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "barrier.cta.red.and.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -52,10 +52,10 @@ extern "C" {
 #define GBATTN_OK 0
 #define GBATTN_EBADSHAPE (-1)       /* B, H, Hkv, Sq, Sk (or Sk_max) < 1, or a size overflows */
 #define GBATTN_EHEADS (-2)          /* H % Hkv != 0 (M4.4 0x06A admissibility) */
-#define GBATTN_EHEADDIM (-3)        /* d not in {64, 128} */
+#define GBATTN_EHEADDIM (-3)        /* d not in {64, 128} (attn_bwd: d != 128) */
 #define GBATTN_EDTYPE (-4)          /* dtype is neither GBATTN_F16 nor GBATTN_BF16 */
 #define GBATTN_EPOINTER (-5)        /* a required pointer is NULL or not 16-byte aligned */
-#define GBATTN_EWORKSPACE (-6)      /* decode workspace smaller than attn_decode_workspace_bytes() */
+#define GBATTN_EWORKSPACE (-6)      /* workspace smaller than the matching *_workspace_bytes() */
 #define GBATTN_ELAUNCH (-7)         /* the CUDA runtime rejected a launch or a tensor map */
 #define GBATTN_EDEVICE_TIMEOUT (-8) /* a kernel's bounded wait gave up (gbattn_device_status) */
 #define GBATTN_ESPLIT (-9)          /* decode n_split < 1 or > 256 */
@@ -132,6 +132,50 @@ int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
                         int B, int Hq, int Hkv, int Sk_max, int d, float scale,
                         int n_split, void *workspace, size_t workspace_bytes,
                         int dtype, void *stream);
+
+/*
+ * attn_bwd_workspace_bytes -- bytes of device workspace attn_bwd needs: the
+ * fp32 row scalars D [B, H, Sq] (rounded up to 256 bytes) followed by the fp32
+ * dQ accumulator [B, H, Sq, d].  For B=1, H=32, Sq=4096, d=128 this is the
+ * 0.5 MiB + 64 MiB of the scratch ledger in M4.4 0x06.1J (the expanded
+ * per-query-head dK/dV buffers of that ledger are not needed here).
+ * Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int Sq, int d);
+
+/*
+ * attn_bwd -- exact attention backward (gradients of attn_fwd).
+ *
+ *   q, o, dout [B, H,   Sq, d]  dtype, inputs (o is attn_fwd's output for q, k, v)
+ *   k, v       [B, Hkv, Sk, d]  dtype, inputs
+ *   lse        [B, H,   Sq]     fp32, input: attn_fwd's LSE (natural log)
+ *   dq         [B, H,   Sq, d]  dtype, output
+ *   dk, dv     [B, Hkv, Sk, d]  dtype, output: summed over the H/Hkv query
+ *              heads that read each KV head
+ *   scale, causal: as passed to attn_fwd
+ *   workspace, workspace_bytes: caller-owned device scratch of at least
+ *              attn_bwd_workspace_bytes(B, H, Sq, d) bytes, 16-byte aligned;
+ *              its contents on entry do not matter
+ *
+ * Definition (M4.4 0x06.1A): with P_ij = exp(scale q_i.k_j - LSE_i) over the
+ * visible keys, dP = dO V^T, D_i = dO_i . O_i, dS = P o (dP - D),
+ * dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.  Three kernels run in
+ * stream order (0x06.1D): D and a zeroed fp32 dQ accumulator; one CTA per
+ * (128-key tile, batch, KV head) that keeps the tile's dK, dV in tensor
+ * memory over every visible query block of every query head in the group
+ * (0x06.1B column owner; the GQA sum of 0x06.1H happens in the accumulator)
+ * and adds each block's dQ into the accumulator with asynchronous fp32
+ * reduce-adds (0x06.1F: atomic, unordered -- dQ is not bitwise repeatable);
+ * then the conversion of dQ to dtype.
+ *
+ * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM (d must be 128), EDTYPE,
+ * EPOINTER (every pointer required; lse 4-byte aligned), EWORKSPACE,
+ * EUNSUPPORTED, ELAUNCH.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             const void *dout, void *dq, void *dk, void *dv,
+             int B, int H, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+             void *workspace, size_t workspace_bytes, int dtype, void *stream);
 
 /*
  * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot

@@ -33,3 +33,33 @@ def assert_attn_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
             lerr = np.abs(lse[~inf_ref] - lse_ref[~inf_ref])
             assert lerr.max() <= LSE_MAX_ABS, f"{what}: LSE max-abs {lerr.max():.3e} > {LSE_MAX_ABS}"
     return float(err.max()), float(err.mean())
+
+
+# Gradient tolerances (backward), relative to each gradient tensor's own scale:
+# relative Frobenius error <= 1e-2 and every element within 2e-2 * max|ref|.
+# The kernel rounds P and dS to the input dtype before the tensor-core
+# products (relative 2^-9 for bf16, each term), takes D = dO . O from the
+# forward's rounded O, and rounds dQ/dK/dV to the dtype (2^-9): each source
+# alone is a ~0.1-0.2 % relative error; the bounds leave a 5x margin.
+GRAD_REL_FRO = 1e-2
+GRAD_MAX_REL = 2e-2
+# Absolute floor for gradients whose exact value is (near) zero, e.g. dQ with a
+# single visible key: the kernel's D = dO . O (fp32 FMA chain over d) and its
+# dP (tensor-core fp32 sums) differ by ~d * 2^-24 * |dO||O|, so dS and dQ carry
+# an absolute error of about tau * that * max|K| ~ 1e-6 even where they vanish.
+GRAD_ATOL = 1e-5
+
+
+def assert_grad_close(g_gpu, g_ref, what=""):
+    g = g_gpu.detach().float().cpu().numpy().astype(np.float64) if isinstance(g_gpu, torch.Tensor) \
+        else np.asarray(g_gpu, dtype=np.float64)
+    ref = np.asarray(g_ref, dtype=np.float64).reshape(g.shape)
+    assert np.isfinite(g).all(), f"{what}: non-finite gradient"
+    scale = np.abs(ref).max()
+    err = np.abs(g - ref)
+    fro = np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300)
+    fro_bound = GRAD_REL_FRO + GRAD_ATOL * np.sqrt(ref.size) / max(np.linalg.norm(ref), 1e-300)
+    assert fro <= fro_bound, f"{what}: relative Frobenius error {fro:.3e} > {fro_bound:.3e}"
+    assert err.max() <= GRAD_MAX_REL * scale + GRAD_ATOL, \
+        f"{what}: max-abs {err.max():.3e} > {GRAD_MAX_REL} x max|ref| ({scale:.3e})"
+    return float(fro), float(err.max() / max(scale, 1e-300))

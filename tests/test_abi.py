@@ -127,3 +127,37 @@ def test_causal_planner_bottom_right_rectangles(lib):
     # the 8192-token causal prefill with 128 x 128 tiles visits 2,080 of 4,096 tiles
     got = binding.gbattn_causal_tile_counts(8192, 8192, 128, 128)
     assert got["full"] + got["partial"] == 2080 and got["partial"] == 64
+
+
+def _bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, H=4,
+             Hkv=2, Sq=8, Sk=8, d=128, scale=0.1, causal=1, ws=FAKE, wsb=1 << 20, dtype=1, stream=None)
+    a.update(kw)
+    return lib.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
+                        a["B"], a["H"], a["Hkv"], a["Sq"], a["Sk"], a["d"], a["scale"], a["causal"],
+                        a["ws"], a["wsb"], a["dtype"], a["stream"])
+
+
+def test_bwd_workspace_matches_page_ledger(lib, golden):
+    """The backward workspace is the fp32 dQ accumulator plus the row scalars
+    D: at the ledger coordinate of M4.4 0x06.1J that is 64 MiB + 0.5 MiB."""
+    g = golden("bwd_scratch_ledger.json")
+    c = g["coordinate"]
+    mib = 1 << 20
+    want = (g["objects_mib"]["dQaccum"] + g["objects_mib"]["D"]) * mib
+    assert lib.attn_bwd_workspace_bytes(c["B"], c["Hq"], c["Sq"], c["d"]) == want
+    assert lib.attn_bwd_workspace_bytes(0, 1, 1, 128) == 0
+
+
+def test_bwd_validation(lib):
+    assert _bwd(lib, B=0) == -1
+    assert _bwd(lib, Sk=0) == -1
+    assert _bwd(lib, H=6, Hkv=4) == -2
+    assert _bwd(lib, d=64) == -3
+    assert _bwd(lib, dtype=2) == -4
+    for name in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv", "ws"):
+        assert _bwd(lib, **{name: None}) == -5, name
+    assert _bwd(lib, dq=FAKE + 8) == -5
+    assert _bwd(lib, lse=FAKE + 2) == -5
+    need = lib.attn_bwd_workspace_bytes(1, 4, 8, 128)
+    assert _bwd(lib, wsb=need - 1) == -6
