@@ -49,6 +49,8 @@ DECODE = WORKLOADS["decode_splitkv_bf16_b64_hq32_hkv8_sk32768_d128"]
 # (the tiny one is a parity case only: a few microseconds per launch).
 OTHER_PREFILL = [WORKLOADS["prefill_fp16_b1_h8_s4096_d64"],
                  WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"]]
+# Backward workloads (d = 128), measured in the default run under "backward".
+BACKWARD = [WORKLOADS["causal_bf16_b4_h16_s8192_d128"], WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"]]
 PREFILL_METRIC = "attention fwd TFLOP/s (% BF16 tensor peak)"
 DECODE_METRIC = "decode HBM GB/s (% peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -419,6 +421,56 @@ def bench_decode(args, world, rank, peaks, peak_kind, steps=None, warmup=None):
     }
 
 
+def bench_backward(args, world, rank, peaks, peak_kind, w=None, steps=None, warmup=None):
+    """attn_bwd on a forward workload: O and LSE from one attn_fwd call (not
+    timed), then preprocess + main + dQ conversion timed per step.  FLOPs:
+    the pages' convention of 2.5x the forward (five matmul-shaped products
+    instead of two), i.e. 10*B*H*Sq*Sk*d, halved for causal."""
+    from exact_tiled_attention_gb300 import (attn_bwd, attn_bwd_workspace_bytes, attn_fwd,
+                                             gbattn_device_status)
+    from exact_tiled_attention_gb300.inputs import make_generator, randn
+
+    w = w or PREFILL
+    steps = steps or args.steps
+    warmup = warmup if warmup is not None else args.warmup
+    stream = torch.cuda.current_stream()
+    q, k, v = make_workload(w, device="cuda")
+    do = randn(q.shape, q.dtype, make_generator(w.seed + 100, "cuda"), "cuda")
+    o, lse = attn_fwd(q, k, v, scale=w.scale, causal=w.causal, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(attn_bwd_workspace_bytes(w.B, w.H, w.Sq, w.d), dtype=torch.uint8, device="cuda")
+    run = lambda: attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, workspace=ws,  # noqa: E731
+                           dq=dq, dk=dk, dv=dv, stream=stream)
+    footprint = 9 * q.numel() * 2 + ws.numel()
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    if footprint < 2 * L2_BYTES:
+        flush_buf = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+        secs = time_steps_flushed(run, steps, warmup, world, stream, flush_buf)
+        del flush_buf
+        l2_note = "L2 flushed before every call (516 MB write outside the event interval)"
+    else:
+        secs = time_steps(run, steps, warmup, world, stream)
+        l2_note = f"inputs, outputs and workspace {footprint / 1e6:.0f} MB > 129 MB L2; no flush"
+    clocks = sampler.stop()
+    if gbattn_device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout")
+    secs = max_over_ranks(secs, world)
+    flops = 2.5 * prefill_flops(w)
+    per_call = secs / steps
+    achieved = flops / per_call / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"metric": "attention bwd TFLOP/s (% BF16 tensor peak)", "workload": w.name,
+            "value": round(flops * steps * world / secs / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_call": round(per_call * 1e3, 4), "steps": steps, "warmup": warmup,
+            "flops_per_call": flops, "flop_convention": "2.5 x forward (10*B*H*Sq*Sk*d, /2 causal)",
+            "kernels_per_call": 3,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_kind": f"{peak_kind} bf16 burst; time of all three kernels"},
+            "l2": l2_note, "clocks": clocks}
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def cpu_oracle_prefill(target_seconds: float, w=None):
     """Time the fp64 oracle on whole heads of the prefill workload (every
@@ -554,6 +606,8 @@ def main():
     ap.add_argument("--impl", choices=["gbattn", "reference"], default="gbattn")
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "decode"] + [n for n, w in WORKLOADS.items() if not w.decode])
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only attn_bwd on the headline forward workload (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -584,6 +638,20 @@ def main():
     from exact_tiled_attention_gb300 import load_library
 
     load_library()  # fail loudly if the CUDA library is missing
+    if args.backward_only:
+        w2 = PREFILL if args.workload == "prefill" else WORKLOADS[args.workload]
+        if args.batch > 0:
+            import dataclasses
+
+            w2 = dataclasses.replace(w2, B=args.batch)
+        line = bench_backward(args, world, rank, peaks, peak_kind, w=w2)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
     if args.workload == "prefill":
         line = bench_prefill(args, world, rank, peaks, peak_kind)
         if not args.no_secondary:
@@ -591,6 +659,9 @@ def main():
                                           steps=max(3, min(args.steps, 20)), warmup=3)
             line["prefill_other"] = [bench_prefill(args, world, rank, peaks, peak_kind, w=w2,
                                                    with_e2e=False) for w2 in OTHER_PREFILL]
+            bw_steps = max(3, min(args.steps, 20))
+            line["backward"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
+                                               warmup=3) for w2 in BACKWARD]
     elif args.workload in WORKLOADS and not WORKLOADS[args.workload].decode:
         w2 = WORKLOADS[args.workload]
         if args.batch > 0:

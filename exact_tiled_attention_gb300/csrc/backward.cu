@@ -40,7 +40,7 @@
 //   warps 0-3  "P" warpgroup: thread = key row; P^T, dS^T; then dV epilogue
 //   warps 4-7  "Q" warpgroup: thread = column d of dQ^T; dQ drain through a
 //              shared staging tile + bulk reduce-add; then dK epilogue
-//   warp  8    loader: K, V once (TMA), Q_t/dO_t per block (TMA, 2 stages),
+//   warp  8    loader: K, V once (TMA), Q_t/dO_t per block (TMA, 3 stages),
 //              per-row LSE (in base 2) and D (plain loads by all 32 lanes)
 //   warp  9    TMEM allocation; lane 0 issues every MMA and commit
 //
@@ -58,7 +58,7 @@ namespace {
 constexpr int kD = 128;       // head dimension of this kernel
 constexpr int kBN = 128;      // keys per CTA (TMEM lanes)
 constexpr int kBM = 64;       // query rows per block
-constexpr int kStages = 2;    // Q/dO stages
+constexpr int kStages = 3;    // Q/dO stages
 constexpr int kThreads = 320;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -104,7 +104,7 @@ struct __align__(8) BwdBars {
   uint64_t qd_empty[kStages];
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t dp_full;
+  uint64_t dp_full, dp_free;
   uint64_t p_full, p_free;
   uint64_t ds_full, ds_free;
   uint64_t dq_full, dq_free;
@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_free[x], 128);
     }
     mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 128);
     mbar_init(&bars->p_full, 128);
     mbar_init(&bars->p_free, 1);
     mbar_init(&bars->ds_full, 128);
@@ -329,21 +330,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         issue_acc(kColDV, dP_A, aDO0 + s * kQBytes, t > 0);
         mma_commit(&bars->p_free);
+        // dP^T of the next block as soon as dP^T(t) is in registers, so the
+        // P warpgroup can form dS(t+1) while dK(t) and dQ(t) run
+        if (t + 1 < T) {
+          if (!(ok = wait_bar(&bars->dp_free, t & 1, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_scores(kColDP, dV_A, aDO0 + ((t + 1) % kStages) * kQBytes);
+          mma_commit(&bars->dp_full);
+        }
         // dK += dS^T Q_t ; dQ_t^T = K^T dS^T
         if (!(ok = wait_bar(&bars->ds_full, t & 1, abort_flag, p.status))) break;
         tc_fence_after();
         issue_acc(kColDK, dDS_A, aQ0 + s * kQBytes, t > 0);
+        mma_commit(&bars->qd_empty[s]);  // last reader of Q_t and dO_t
         if (t >= 1 && !(ok = wait_bar(&bars->dq_free, (t - 1) & 1, abort_flag, p.status))) break;
         tc_fence_after();
         issue_dq();
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free);
-        mma_commit(&bars->qd_empty[s]);
-        // dP^T of the next block (its TMEM columns were read before ds_full)
-        if (t + 1 < T) {
-          issue_scores(kColDP, dV_A, aDO0 + ((t + 1) % kStages) * kQBytes);
-          mma_commit(&bars->dp_full);
-        }
       }
       mma_commit(&bars->acc_done);
       // Every MMA issued must complete before TMEM is released.
@@ -390,11 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need_mask = (k0 + kBN > p.Sk) || (CAUSAL && (k0 + kBN - 1 > q0 + p.delta));
       const int first_c = (key >= p.Sk) ? kBM : (CAUSAL ? key - p.delta - q0 : 0);
       float pr[kBM];
+      const float4* sl4 = reinterpret_cast<const float4*>(st);
 #pragma unroll
-      for (int c = 0; c < kBM; ++c) {
-        float x = ex2_approx(fmaf(__uint_as_float(u[c]), lam, -st[c]));
-        if (need_mask && c < first_c) x = 0.f;
-        pr[c] = x;
+      for (int c4 = 0; c4 < kBM / 4; ++c4) {
+        const float4 l4 = sl4[c4];  // base-2 LSE of rows 4c4 .. 4c4+3 (broadcast read)
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = 4 * c4 + i;
+          float x = ex2_approx(fmaf(__uint_as_float(u[c]), lam, -lv[i]));
+          if (need_mask && c < first_c) x = 0.f;
+          pr[c] = x;
+        }
       }
       if (t >= 1) {
         ok = wait_bar(&bars->p_free, (t - 1) & 1, abort_flag, p.status);
@@ -426,8 +437,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
       reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
       tc_fence_before();
+      mbar_arrive(&bars->dp_free);
+      const float4* st4 = reinterpret_cast<const float4*>(st + kBM);
 #pragma unroll
-      for (int c = 0; c < kBM; ++c) pr[c] = pr[c] * (__uint_as_float(u[c]) - st[kBM + c]);
+      for (int c4 = 0; c4 < kBM / 4; ++c4) {
+        const float4 dd = st4[c4];  // D of rows 4c4 .. 4c4+3 (broadcast read)
+        pr[4 * c4 + 0] *= __uint_as_float(u[4 * c4 + 0]) - dd.x;
+        pr[4 * c4 + 1] *= __uint_as_float(u[4 * c4 + 1]) - dd.y;
+        pr[4 * c4 + 2] *= __uint_as_float(u[4 * c4 + 2]) - dd.z;
+        pr[4 * c4 + 3] *= __uint_as_float(u[4 * c4 + 3]) - dd.w;
+      }
       if (t >= 1) {
         ok = wait_bar(&bars->ds_free, (t - 1) & 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) {
