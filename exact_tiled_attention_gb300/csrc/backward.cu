@@ -8,45 +8,57 @@
 //     dS_ij = P_ij (dP_ij - D_i)
 //     dQ = tau dS K,   dK = tau dS^T Q,   dV = P^T dO
 //
-// Three kernels in stream order (the producer graph of 0x06.1D):
-//   1. bwd_preprocess_kernel: D = rowsum(dO * O) in fp32 and a zeroed fp32
-//      dQ accumulator;
-//   2. bwd_main_kernel: one CTA owns a 128-key tile of one (batch, KV head)
-//      -- the column owner of 0x06.1B -- and loops over every visible 64-row
-//      query block of EVERY query head that reads this KV head.  dK and dV of
-//      the tile accumulate in tensor memory across the whole loop, so the
-//      grouped-query sum of 0x06.1H happens in the accumulator and no
-//      expanded per-query-head dK/dV buffers or group-sum pass exist.  Each
-//      block's dQ contribution is added to the fp32 accumulator in global
-//      memory with one bulk asynchronous reduce-add (atomic per element, no
-//      fixed order: 0x06.1F);
-//   3. bwd_dq_convert_kernel: dQ accumulator (already scaled by tau) -> dtype.
+// Section 0x06.1C: dQ reduces over key tiles, dK/dV over query tiles, and no
+// single owner makes all three single-writer.  Instead of the column owner
+// with fp32 atomic dQ of 0x06.1D, each reduction gets its own owner (both
+// owners are named in 0x06.1C / 0x06.1I; the scores are recomputed by each):
+//   1. bwd_preprocess_kernel: D = rowsum(dO * O) in fp32;
+//   2. bwd_dkdv_kernel, the column owner: one CTA per 128-key tile of one
+//      (batch, KV head) loops over every visible 128-row query block of EVERY
+//      query head that reads this KV head; dK and dV accumulate in tensor
+//      memory, so the grouped-query sum of 0x06.1H happens in the
+//      accumulator (no expanded per-query-head buffers, no group-sum pass);
+//   3. bwd_dq_kernel, the row owner: one CTA per 128-row query block of one
+//      (batch, query head) loops over every visible key tile; dQ accumulates
+//      in tensor memory.
+// Every gradient element has one writer and a fixed summation order, so the
+// result is bitwise repeatable and no fp32 scratch beyond D is needed.  The
+// price is two more 128 x 128 products per (query block, key tile) pair
+// (S and dP are formed by both owners): seven instead of five.
 //
-// Main kernel, per query block t (64 rows of query head h), all five
-// contractions on tcgen05 with fp32 accumulation in tensor memory; the key
-// axis is the TMEM lane axis, so each thread of the "P" warpgroup owns one
-// key row of the transposed score tile:
-//     S^T  = K Q_t^T          M=128 keys, N=64 rows, K=d     (SS, K-major)
-//     dP^T = V dO_t^T         M=128 keys, N=64 rows, K=d     (SS, K-major)
-//     dV  += P^T dO_t         M=128 keys, N=d, K=64 rows     (A K-major, B MN-major)
-//     dK  += dS^T Q_t         M=128 keys, N=d, K=64 rows     (A K-major, B MN-major)
-//     dQ_t^T = K^T dS^T       M=d, N=64 rows, K=128 keys     (A and B MN-major)
-// P^T and dS^T are rounded to the input dtype and staged in shared memory
-// (K-major for dV/dK, read MN-major by the dQ^T product -- one buffer serves
-// both).  Tensor memory (512 columns): dV [0,128), dK [128,256),
-// S^T two buffers [256,320) [320,384), dP^T [384,448), dQ^T [448,512).
+// Column owner, per query block t (128 rows of query head h); the key axis
+// is the TMEM lane axis, each thread of the two "P" warpgroups owns one key
+// row and 64 of the block's 128 query columns:
+//     S^T  = K Q_t^T       A = K (smem, K-major),    B = Q_t (smem, K-major)
+//     dP^T = V dO_t^T      A = V (smem, K-major),    B = dO_t (smem, K-major)
+//     dV  += P^T dO_t      A = P^T (tensor memory),  B = dO_t (smem, MN-major)
+//     dK  += dS^T Q_t      A = dS^T (tensor memory), B = Q_t (smem, MN-major)
+//   P^T / dS^T (input dtype) overwrite the fp32 S^T / dP^T they came from.
+//   TMEM: dV [0,128), dK [128,256), S^T/P^T [256,384), dP^T/dS^T [384,512).
 //
-// Roles (320 threads):
-//   warps 0-3  "P" warpgroup: thread = key row; P^T, dS^T; then dV epilogue
-//   warps 4-7  "Q" warpgroup: thread = column d of dQ^T; dQ drain through a
-//              shared staging tile + bulk reduce-add; then dK epilogue
-//   warp  8    loader: K, V once (TMA), Q_t/dO_t per block (TMA, 3 stages),
-//              per-row LSE (in base 2) and D (plain loads by all 32 lanes)
-//   warp  9    TMEM allocation; lane 0 issues every MMA and commit
+// Row owner, per key tile j; the query axis is the TMEM lane axis, each
+// thread of the two softmax warpgroups owns one query row and 64 of the
+// tile's 128 keys:
+//     S    = Q K_j^T       A = Q (tensor memory),    B = K_j (smem, K-major)
+//     dP   = dO V_j^T      A = dO (tensor memory),   B = V_j (smem, K-major)
+//     dQ  += dS K_j        A = dS (tensor memory),   B = K_j (smem, MN-major)
+//   Q and dO are written to tensor memory once per CTA; dS (input dtype)
+//   overwrites the fp32 dP it came from.
+//   TMEM: dQ [0,128), S [128,256), dP/dS [256,384), Q [384,448), dO [448,512).
 //
-// Causal (bottom-right delta = Sk - Sq): query rows that cannot see the tile's
-// first key are never visited; blocks crossing the diagonal and the key /
-// query tails are masked element-wise before the exponential.
+// A 128 x 128 x 16 MMA with both operands in shared memory is bound by the
+// shared-memory operand reads (two 4 KiB operands per ~70 cycles, measured);
+// every product above with an operand in tensor memory reads only one.
+//
+// Roles (384 threads, three warpgroups; setmaxnreg 184 / 184 / 136):
+//   warps 0-7   two compute warpgroups (columns [0,64) and [64,128))
+//   warp  8     loader (TMA; the column owner's loader lanes also stage the
+//               block's row statistics in shared memory)
+//   warp  9     TMEM allocation; lane 0 issues every MMA and commit
+//
+// Causal (bottom-right delta = Sk - Sq): tiles wholly in the future are never
+// visited; tiles crossing the diagonal and the key / query tails are masked
+// element-wise before the exponential.
 #include <cuda_runtime.h>
 
 #include "gbattn_internal.h"
@@ -55,62 +67,30 @@
 namespace gbattn {
 namespace {
 
-constexpr int kD = 128;       // head dimension of this kernel
-constexpr int kBN = 128;      // keys per CTA (TMEM lanes)
-constexpr int kBM = 64;       // query rows per block
-constexpr int kStages = 3;    // Q/dO stages
-constexpr int kThreads = 320;
+constexpr int kD = 128;      // head dimension of these kernels
+constexpr int kT = 128;      // rows (keys or queries) per tile
+constexpr int kThreads = 384;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kRegsCompute = 184, kRegsCtl = 136;
+static_assert(2 * 128 * kRegsCompute + 128 * kRegsCtl <= kThreads * 168, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared memory (offsets from a 1024-byte aligned base).
-constexpr int kKBytes = kBN * kD * 2;        // 32 KiB: two 128-row x 128-byte column blocks
-constexpr int kKBlock = kBN * 128;           // 16 KiB
-constexpr int kQBytes = kBM * kD * 2;        // 16 KiB: two 64-row x 128-byte column blocks
-constexpr int kQBlock = kBM * 128;           // 8 KiB
-constexpr int kPBytes = kBN * kBM * 2;       // 16 KiB: 128 key rows x 128 bytes
-constexpr int kStageBytes = kBM * kD * 4;    // 32 KiB fp32 dQ staging tile
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kKBytes;
-constexpr int kOffQ = kOffV + kKBytes;                 // kStages tiles
-constexpr int kOffDO = kOffQ + kStages * kQBytes;      // kStages tiles
-constexpr int kOffP = kOffDO + kStages * kQBytes;
-constexpr int kOffDS = kOffP + kPBytes;
-constexpr int kOffStage = kOffDS + kPBytes;
-constexpr int kOffStats = kOffStage + kStageBytes;     // kStages x (64 lse2 + 64 D) floats
-constexpr int kOffBars = kOffStats + kStages * 2 * kBM * 4;
-constexpr int kSmemBytes = 1024 + kOffBars + 256;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-// TMEM columns
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS0 = 256, kColDP = 384, kColDQ = 448;
+constexpr int kTileBytes = kT * kD * 2;  // 32 KiB: 128 rows x 128 16-bit columns
+constexpr int kBlock = kT * 128;         // 16 KiB: 128 rows x one 128-byte column block
 
 struct BwdParams {
   const float* lse;   // [B,H,Sq] natural log
   const float* Dvec;  // [B,H,Sq]
-  float* dq_acc;      // [B,H,Sq,D] fp32
+  const void* q;      // [B,H,Sq,D]   (row owner: Q and dO rows into TMEM)
+  const void* dout;
+  void* dq;           // [B,H,Sq,D]
   void* dk;           // [B,Hkv,Sk,D]
   void* dv;
   int B, H, Hkv, Sq, Sk, g;
-  int n_ktiles, head_group, delta;
+  int n_ktiles, n_qtiles, head_group, delta;
   float scale, scale_log2;
   int* status;
-};
-
-struct __align__(8) BwdBars {
-  uint64_t kv_full;
-  uint64_t qd_full[kStages];
-  uint64_t qd_empty[kStages];
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t dp_full, dp_free;
-  uint64_t p_full, p_free;
-  uint64_t ds_full, ds_free;
-  uint64_t dq_full, dq_free;
-  uint64_t acc_done;
-  uint32_t tmem_base;
-  int abort_flag;
 };
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -118,22 +98,69 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return bounded_wait(bar, parity, abort_flag, status, kStatusTimeoutBwd);
 }
 
+// Descriptor K-steps.  K-major: a step of 16 elements adds 32 bytes inside a
+// 128-byte row, or jumps a 16 KiB column block.  MN-major (leading offset =
+// 16 KiB between 64-element column blocks, stride offset = 8 rows of 128
+// bytes): a step of 16 rows adds 2048 bytes.
+__device__ __forceinline__ uint64_t kstep_kmajor(int kk) {
+  return static_cast<uint64_t>(((kk / 4) * kBlock + (kk % 4) * 32) >> 4);
+}
+__device__ __forceinline__ uint64_t kstep_mnmajor(int kk) { return static_cast<uint64_t>((kk * 2048) >> 4); }
+
+// Rounds 32 fp32 values x[base .. base+32) to 16 packed 16-bit pairs
+// (element 2i in the low half).
+template <bool BF16>
+__device__ __forceinline__ void pack32(const float (&x)[64], int base, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(x[base + 2 * i], x[base + 2 * i + 1]);
+}
+
+// =========================================================================
+// Column owner: dK, dV.
+// =========================================================================
+namespace col {
+constexpr int kStages = 2;
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTileBytes;
+constexpr int kOffQ = kOffV + kTileBytes;                 // kStages tiles
+constexpr int kOffDO = kOffQ + kStages * kTileBytes;      // kStages tiles
+constexpr int kOffStats = kOffDO + kStages * kTileBytes;  // kStages x (128 lse2 + 128 D) fp32
+constexpr int kOffBars = kOffStats + kStages * 2 * kT * 4;
+constexpr int kSmemBytes = 1024 + kOffBars + 256;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kColDV = 0, kColDK = 128, kColX = 256, kColY = 384;
+
+struct __align__(8) Bars {
+  uint64_t kv_full;
+  uint64_t qd_full[kStages];
+  uint64_t qd_empty[kStages];
+  uint64_t s_full, dp_full;
+  uint64_t p_full, ds_full;
+  uint64_t dv_done, dk_done;
+  uint64_t acc_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+}  // namespace col
+
 template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_main_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
                     const __grid_constant__ CUtensorMap tmap_do, const BwdParams p) {
+  using namespace col;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem + kOffBars);
-  float* stats = reinterpret_cast<float*>(smem + kOffStats);  // [stage][lse2 64 | D 64]
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+  float* stats = reinterpret_cast<float*>(smem + kOffStats);  // [stage][lse2 128 | D 128]
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
   // ---- work unit: (batch * Hkv + kv head, key tile).  CTAs run in groups of
-  // p.head_group KV heads (their Q/dO/dQ working set stays in L2); inside a
+  // p.head_group KV heads (their Q/dO working set stays in L2); inside a
   // group, key tiles ascend (causal: the tiles with the most query blocks
   // first) and heads vary fastest.
   const int BHkv = p.B * p.Hkv;
@@ -144,35 +171,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int jt = r_in / heads_here;
   const int b = bkv / p.Hkv;
   const int kvh = bkv % p.Hkv;
-  const int k0 = jt * kBN;
-  const int nqb = (p.Sq + kBM - 1) / kBM;
+  const int k0 = jt * kT;
+  const int nqb = p.n_qtiles;
   int i_start = 0;
   if (CAUSAL) {
     const int q_min = k0 - p.delta;  // first query row that sees key k0
-    i_start = q_min <= 0 ? 0 : (q_min >= p.Sq ? nqb : q_min / kBM);
+    i_start = q_min <= 0 ? 0 : (q_min >= p.Sq ? nqb : q_min / kT);
   }
   const int n_blk = nqb - i_start;
   const int T = p.g * n_blk;  // query blocks this CTA visits
 
-  // ---- setup
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bars->qd_full[s], 1 + 32);  // TMA arrive + 32 lanes' stat stores
       mbar_init(&bars->qd_empty[s], 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&bars->s_full[x], 1);
-      mbar_init(&bars->s_free[x], 128);
-    }
+    mbar_init(&bars->s_full, 1);
     mbar_init(&bars->dp_full, 1);
-    mbar_init(&bars->dp_free, 128);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->p_free, 1);
-    mbar_init(&bars->ds_full, 128);
-    mbar_init(&bars->ds_free, 1);
-    mbar_init(&bars->dq_full, 1);
-    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->dv_done, 1);
+    mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->acc_done, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -195,44 +215,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto block_coords = [&](int t, int& h, int& q0) {
     const int hh = t / n_blk;
     h = kvh * p.g + hh;
-    q0 = (i_start + (t - hh * n_blk)) * kBM;
+    q0 = (i_start + (t - hh * n_blk)) * kT;
   };
 
-  if (warp == kLoadWarp) {
-    // ================================================================ loader
-    int issued = 0;
-    if (T > 0) {
+  if (warp >= kLoadWarp) {
+    regs_dec<kRegsCtl>();
+    if (warp == kLoadWarp && T > 0) {
+      // ============================================================== loader
+      const uint64_t once = policy_evict_first();  // K/V: read by this CTA only
+      const uint64_t reuse = policy_evict_last();  // Q/dO: re-read by every key tile
       if (lane == 0) {
-        const uint64_t keep = policy_evict_first();  // K/V: read by this CTA only
-        mbar_arrive_expect_tx(&bars->kv_full, 2 * kKBytes);
+        mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
         for (int cb = 0; cb < 2; ++cb) {
-          tma_load_3d(smem + kOffK + cb * kKBlock, &tmap_k, &bars->kv_full, cb * 64, k0, bkv, keep);
-          tma_load_3d(smem + kOffV + cb * kKBlock, &tmap_v, &bars->kv_full, cb * 64, k0, bkv, keep);
+          tma_load_3d(smem + kOffK + cb * kBlock, &tmap_k, &bars->kv_full, cb * 64, k0, bkv, once);
+          tma_load_3d(smem + kOffV + cb * kBlock, &tmap_v, &bars->kv_full, cb * 64, k0, bkv, once);
         }
       }
-      const uint64_t reuse = policy_evict_last();  // Q/dO: re-read by every key tile
+      int issued = 0;
       for (int t = 0; t < T; ++t) {
         const int s = t % kStages;
-        const uint32_t ph = (t / kStages) & 1;
-        bool ok = wait_bar(&bars->qd_empty[s], ph ^ 1, abort_flag, p.status);
+        const bool ok = wait_bar(&bars->qd_empty[s], ((t / kStages) & 1) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) break;
         int h, q0;
         block_coords(t, h, q0);
-        const long long row0 = (static_cast<long long>(b) * p.H + h) * p.Sq;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * kQBytes);
+          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * kTileBytes);
           for (int cb = 0; cb < 2; ++cb) {
-            tma_load_3d(smem + kOffQ + s * kQBytes + cb * kQBlock, &tmap_q, &bars->qd_full[s], cb * 64,
+            tma_load_3d(smem + kOffQ + s * kTileBytes + cb * kBlock, &tmap_q, &bars->qd_full[s], cb * 64,
                         q0, b * p.H + h, reuse);
-            tma_load_3d(smem + kOffDO + s * kQBytes + cb * kQBlock, &tmap_do, &bars->qd_full[s],
+            tma_load_3d(smem + kOffDO + s * kTileBytes + cb * kBlock, &tmap_do, &bars->qd_full[s],
                         cb * 64, q0, b * p.H + h, reuse);
           }
         }
-        // per-row statistics: LSE in base 2 (+inf for rows past Sq or rows
-        // with no visible key, so that their P is exactly 0) and D
-        float* st = stats + s * 2 * kBM;
+        // Row statistics of the block: LSE in base 2 (+inf for rows past Sq
+        // and rows with no visible key, so that their P is exactly 0) and D.
+        const long long row0 = (static_cast<long long>(b) * p.H + h) * p.Sq;
+        float* st = stats + s * 2 * kT;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           const int c = lane + 32 * u;
           const int row = q0 + c;
           float l2 = INFINITY, dv = 0.f;
@@ -242,309 +262,195 @@ __global__ void __launch_bounds__(kThreads, 1)
             dv = p.Dvec[row0 + row];
           }
           st[c] = l2;
-          st[kBM + c] = dv;
+          st[kT + c] = dv;
         }
         mbar_arrive(&bars->qd_full[s]);
         issued = t + 1;
       }
-    }
-    if (lane == 0 && T > 0) {
-      // Drain: every copy this thread issued must land before exit.
-      int dummy = 0;
-      volatile int* no_abort = reinterpret_cast<volatile int*>(&dummy);
-      bounded_wait(&bars->kv_full, 0, no_abort, p.status, kStatusTimeoutDrain);
-      for (int t = max(0, issued - kStages); t < issued; ++t)
-        bounded_wait(&bars->qd_full[t % kStages], (t / kStages) & 1, no_abort, p.status,
-                     kStatusTimeoutDrain);
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issuer
-    if (lane == 0 && T > 0) {
-      constexpr uint32_t kIdS = idesc_f16(BF16, false, false, kBN, kBM);   // S^T, dP^T
-      constexpr uint32_t kIdAcc = idesc_f16(BF16, false, true, kBN, kD);   // dV, dK
-      constexpr uint32_t kIdDQ = idesc_f16(BF16, true, true, kD, kBM);     // dQ^T
-      const uint32_t aK = smem_u32(smem + kOffK), aV = smem_u32(smem + kOffV);
-      const uint32_t aP = smem_u32(smem + kOffP), aDS = smem_u32(smem + kOffDS);
-      // K-major descriptors (K, V as A; Q, dO as B of the score products; P,
-      // dS as A of the accumulations): a K-step of 16 elements adds 32 bytes
-      // inside a 128-byte row, or jumps a column block.
-      const uint64_t dK_A = smem_desc_sw128(aK, 16, 1024);
-      const uint64_t dV_A = smem_desc_sw128(aV, 16, 1024);
-      const uint64_t dP_A = smem_desc_sw128(aP, 16, 1024);
-      const uint64_t dDS_A = smem_desc_sw128(aDS, 16, 1024);
-      // MN-major descriptors: leading offset = stride between 64-element
-      // column blocks, stride offset = 8 rows of 128 bytes; a K-step of 16
-      // rows adds 2048 bytes.
-      const uint64_t dKT_A = smem_desc_sw128(aK, kKBlock, 1024);  // K^T for dQ^T
-      const uint64_t dDS_B = smem_desc_sw128(aDS, kKBlock, 1024); // dS^T as B of dQ^T
-
-      auto issue_scores = [&](uint32_t d_col, uint64_t a_desc, uint32_t b_base) {
-        const uint64_t bd = smem_desc_sw128(b_base, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint64_t ao = ((kk / 4) * kKBlock + (kk % 4) * 32) >> 4;
-          const uint64_t bo = ((kk / 4) * kQBlock + (kk % 4) * 32) >> 4;
-          mma_f16_ss(tmem + d_col, a_desc + ao, bd + bo, kIdS, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_acc = [&](uint32_t d_col, uint64_t a_desc, uint32_t b_base, bool accumulate) {
-        const uint64_t bd = smem_desc_sw128(b_base, kQBlock, 1024);
-#pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_f16_ss(tmem + d_col, a_desc + ((kk * 32) >> 4), bd + ((kk * 2048) >> 4), kIdAcc,
-                     (accumulate || kk > 0) ? 1u : 0u);
-      };
-      auto issue_dq = [&]() {
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_f16_ss(tmem + kColDQ, dKT_A + ((kk * 2048) >> 4), dDS_B + ((kk * 2048) >> 4), kIdDQ,
-                     kk > 0 ? 1u : 0u);
-      };
-      const uint32_t aQ0 = smem_u32(smem + kOffQ), aDO0 = smem_u32(smem + kOffDO);
-
-      bool ok = wait_bar(&bars->kv_full, 0, abort_flag, p.status) &&
-                wait_bar(&bars->qd_full[0], 0, abort_flag, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_scores(kColS0, dK_A, aQ0);
-        mma_commit(&bars->s_full[0]);
-        issue_scores(kColDP, dV_A, aDO0);
-        mma_commit(&bars->dp_full);
+      if (lane == 0) {
+        // Drain: every copy this warp issued must land before exit.
+        int dummy = 0;
+        volatile int* no_abort = reinterpret_cast<volatile int*>(&dummy);
+        bounded_wait(&bars->kv_full, 0, no_abort, p.status, kStatusTimeoutDrain);
+        for (int t = max(0, issued - kStages); t < issued; ++t)
+          bounded_wait(&bars->qd_full[t % kStages], (t / kStages) & 1, no_abort, p.status,
+                       kStatusTimeoutDrain);
       }
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t % kStages;
-        if (t + 1 < T) {
-          const int s1 = (t + 1) % kStages;
-          const int sb = (t + 1) & 1;  // S buffer
-          if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / kStages) & 1, abort_flag, p.status))) break;
-          if (t + 1 >= 2 &&
-              !(ok = wait_bar(&bars->s_free[sb], (((t + 1) >> 1) - 1) & 1, abort_flag, p.status)))
-            break;
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ============================================================== MMA issuer
+      if (lane == 0 && T > 0) {
+        constexpr uint32_t kIdSS = idesc_f16(BF16, false, false, 128, 128);  // S^T, dP^T
+        constexpr uint32_t kIdTS = idesc_f16(BF16, false, true, 128, 128);   // dV, dK
+        const uint64_t dK_A = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
+        const uint64_t dV_A = smem_desc_sw128(smem_u32(smem + kOffV), 16, 1024);
+        const uint32_t aQ0 = smem_u32(smem + kOffQ), aDO0 = smem_u32(smem + kOffDO);
+        auto issue_ss = [&](uint32_t d_col, uint64_t a_desc, uint32_t b_base) {
+          const uint64_t bd = smem_desc_sw128(b_base, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_ss(tmem + d_col, a_desc + kstep_kmajor(kk), bd + kstep_kmajor(kk), kIdSS, kk > 0 ? 1u : 0u);
+        };
+        // A from tensor memory: 16 query rows (K) = 8 packed columns; rows
+        // 0-63 sit in columns [0,32) of the region, rows 64-127 in [64,96).
+        auto issue_ts = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base, bool accumulate) {
+          const uint64_t bd = smem_desc_sw128(b_base, kBlock, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_f16_ts(tmem + d_col, tmem + a_col + (kk / 4) * 64 + (kk % 4) * 8, bd + kstep_mnmajor(kk), kIdTS,
+                       (accumulate || kk > 0) ? 1u : 0u);
+        };
+        bool ok = wait_bar(&bars->kv_full, 0, abort_flag, p.status) &&
+                  wait_bar(&bars->qd_full[0], 0, abort_flag, p.status);
+        if (ok) {
           tc_fence_after();
-          issue_scores(kColS0 + sb * kBM, dK_A, aQ0 + s1 * kQBytes);
-          mma_commit(&bars->s_full[sb]);
-        }
-        // dV += P^T dO_t
-        if (!(ok = wait_bar(&bars->p_full, t & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        issue_acc(kColDV, dP_A, aDO0 + s * kQBytes, t > 0);
-        mma_commit(&bars->p_free);
-        // dP^T of the next block as soon as dP^T(t) is in registers, so the
-        // P warpgroup can form dS(t+1) while dK(t) and dQ(t) run
-        if (t + 1 < T) {
-          if (!(ok = wait_bar(&bars->dp_free, t & 1, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_scores(kColDP, dV_A, aDO0 + ((t + 1) % kStages) * kQBytes);
+          issue_ss(kColX, dK_A, aQ0);
+          mma_commit(&bars->s_full);
+          issue_ss(kColY, dV_A, aDO0);
           mma_commit(&bars->dp_full);
         }
-        // dK += dS^T Q_t ; dQ_t^T = K^T dS^T
-        if (!(ok = wait_bar(&bars->ds_full, t & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        issue_acc(kColDK, dDS_A, aQ0 + s * kQBytes, t > 0);
-        mma_commit(&bars->qd_empty[s]);  // last reader of Q_t and dO_t
-        if (t >= 1 && !(ok = wait_bar(&bars->dq_free, (t - 1) & 1, abort_flag, p.status))) break;
-        tc_fence_after();
-        issue_dq();
-        mma_commit(&bars->dq_full);
-        mma_commit(&bars->ds_free);
+        for (int t = 0; ok && t < T; ++t) {
+          const int s = t % kStages;
+          const uint32_t ph = t & 1;
+          // dV += P^T dO_t
+          if (!(ok = wait_bar(&bars->p_full, ph, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_ts(kColDV, kColX, aDO0 + s * kTileBytes, t > 0);
+          mma_commit(&bars->dv_done);
+          // dK += dS^T Q_t (the last reader of this Q/dO stage)
+          if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_ts(kColDK, kColY, aQ0 + s * kTileBytes, t > 0);
+          mma_commit(&bars->dk_done);
+          mma_commit(&bars->qd_empty[s]);
+          if (t + 1 < T) {
+            const int s1 = (t + 1) % kStages;
+            if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / kStages) & 1, abort_flag, p.status))) break;
+            // S^T(t+1) over P^T(t) once dV has read it; dP^T(t+1) over dS^T(t)
+            // once dK has read it
+            if (!(ok = wait_bar(&bars->dv_done, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_ss(kColX, dK_A, aQ0 + s1 * kTileBytes);
+            mma_commit(&bars->s_full);
+            if (!(ok = wait_bar(&bars->dk_done, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_ss(kColY, dV_A, aDO0 + s1 * kTileBytes);
+            mma_commit(&bars->dp_full);
+          }
+        }
+        mma_commit(&bars->acc_done);
+        // Every MMA issued must complete before TMEM is released.
+        int dummy = 0;
+        bounded_wait(&bars->acc_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status,
+                     kStatusTimeoutDrain);
       }
-      mma_commit(&bars->acc_done);
-      // Every MMA issued must complete before TMEM is released.
-      int dummy = 0;
-      bounded_wait(&bars->acc_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status,
-                   kStatusTimeoutDrain);
+      __syncwarp();
     }
-    __syncwarp();
-  } else if (warp < 4) {
-    // ================================================================ P warpgroup
-    const int kl = warp * 32 + lane;  // key row within the tile (= TMEM lane)
+  } else {
+    // ================================================================ P warpgroups
+    regs_inc<kRegsCompute>();
+    const int wg = warp / 4;                // query columns [64 wg, 64 wg + 64) of a block
+    const int kl = (warp % 4) * 32 + lane;  // key row within the tile (= TMEM lane)
     const int key = k0 + kl;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    uint8_t* p_row = smem + kOffP + kl * 128;
-    uint8_t* ds_row = smem + kOffDS + kl * 128;
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t colX = tmem + lane_off + kColX + wg * 64;
+    const uint32_t colY = tmem + lane_off + kColY + wg * 64;
     const float lam = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % kStages;
-      const int sb = t & 1;
+      const uint32_t ph = t & 1;
       int h, q0;
       block_coords(t, h, q0);
       (void)h;
-      // S^T(t) in TMEM; the block's row statistics (plain stores by the
-      // loader, published through qd_full) in shared memory
-      ok = wait_bar(&bars->s_full[sb], (t >> 1) & 1, abort_flag, p.status) &&
+      const int c0 = q0 + wg * 64;  // query row of this warpgroup's first column
+      ok = wait_bar(&bars->s_full, ph, abort_flag, p.status) &&
            wait_bar(&bars->qd_full[s], (t / kStages) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      uint32_t u[kBM];
-      tmem_ld32(tmem + lane_off + kColS0 + sb * kBM, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-      tmem_ld32(tmem + lane_off + kColS0 + sb * kBM + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+      const float4* st_l = reinterpret_cast<const float4*>(stats + s * 2 * kT + wg * 64);
+      const float4* st_d = reinterpret_cast<const float4*>(stats + s * 2 * kT + kT + wg * 64);
+      // One 64-value register row holds S^T, then P^T, then dS^T.
+      float x[64];
+      tmem_ld32(colX, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(colX + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
       tmem_wait_ld();
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-      tc_fence_before();
-      mbar_arrive(&bars->s_free[sb]);
-      const float* st = stats + s * 2 * kBM;
-      // P = 2^(lambda s - LSE log2 e); rows past Sq carry LSE = +inf (P = 0).
-      // Masked: keys past Sk, and (causal) column c with q0 + c + delta < key.
-      const bool need_mask = (k0 + kBN > p.Sk) || (CAUSAL && (k0 + kBN - 1 > q0 + p.delta));
-      const int first_c = (key >= p.Sk) ? kBM : (CAUSAL ? key - p.delta - q0 : 0);
-      float pr[kBM];
-      const float4* sl4 = reinterpret_cast<const float4*>(st);
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      // P = 2^(lambda s - LSE log2 e); masked: keys past Sk, and (causal)
+      // column c with c0 + c + delta < key.
+      const bool need_mask = (k0 + kT > p.Sk) || (CAUSAL && (k0 + kT - 1 > c0 + p.delta));
+      const int first_c = (key >= p.Sk) ? 64 : (CAUSAL ? key - p.delta - c0 : 0);
 #pragma unroll
-      for (int c4 = 0; c4 < kBM / 4; ++c4) {
-        const float4 l4 = sl4[c4];  // base-2 LSE of rows 4c4 .. 4c4+3 (broadcast read)
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = st_l[c4];  // broadcast read
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = 4 * c4 + i;
-          float x = ex2_approx(fmaf(__uint_as_float(u[c]), lam, -lv[i]));
-          if (need_mask && c < first_c) x = 0.f;
-          pr[c] = x;
+          float e = ex2_approx(fmaf(x[c], lam, -lv[i]));
+          if (need_mask && c < first_c) e = 0.f;
+          x[c] = e;
         }
       }
-      if (t >= 1) {
-        ok = wait_bar(&bars->p_free, (t - 1) & 1, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
+      {
+        uint32_t pk[16];
+        pack32<BF16>(x, 0, pk);
+        tmem_st16(colX, pk);  // P^T over this warpgroup's own S^T columns
+        pack32<BF16>(x, 32, pk);
+        tmem_st16(colX + 16, pk);
       }
-#pragma unroll
-      for (int ch = 0; ch < kBM / 8; ++ch) {
-        const uint32_t w0 = pack2<BF16>(pr[ch * 8 + 0], pr[ch * 8 + 1]);
-        const uint32_t w1 = pack2<BF16>(pr[ch * 8 + 2], pr[ch * 8 + 3]);
-        const uint32_t w2 = pack2<BF16>(pr[ch * 8 + 4], pr[ch * 8 + 5]);
-        const uint32_t w3 = pack2<BF16>(pr[ch * 8 + 6], pr[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(p_row + ((ch ^ (kl & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
-      }
-      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
       mbar_arrive(&bars->p_full);
-      // dP^T row -> dS^T row
-      ok = wait_bar(&bars->dp_full, t & 1, abort_flag, p.status);
+      // dP^T -> dS^T, 32 columns at a time
+      ok = wait_bar(&bars->dp_full, ph, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      tmem_ld32(tmem + lane_off + kColDP, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-      tmem_ld32(tmem + lane_off + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-      tmem_wait_ld();
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-      tc_fence_before();
-      mbar_arrive(&bars->dp_free);
-      const float4* st4 = reinterpret_cast<const float4*>(st + kBM);
 #pragma unroll
-      for (int c4 = 0; c4 < kBM / 4; ++c4) {
-        const float4 dd = st4[c4];  // D of rows 4c4 .. 4c4+3 (broadcast read)
-        pr[4 * c4 + 0] *= __uint_as_float(u[4 * c4 + 0]) - dd.x;
-        pr[4 * c4 + 1] *= __uint_as_float(u[4 * c4 + 1]) - dd.y;
-        pr[4 * c4 + 2] *= __uint_as_float(u[4 * c4 + 2]) - dd.z;
-        pr[4 * c4 + 3] *= __uint_as_float(u[4 * c4 + 3]) - dd.w;
-      }
-      if (t >= 1) {
-        ok = wait_bar(&bars->ds_free, (t - 1) & 1, abort_flag, p.status);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-      }
-#pragma unroll
-      for (int ch = 0; ch < kBM / 8; ++ch) {
-        const uint32_t w0 = pack2<BF16>(pr[ch * 8 + 0], pr[ch * 8 + 1]);
-        const uint32_t w1 = pack2<BF16>(pr[ch * 8 + 2], pr[ch * 8 + 3]);
-        const uint32_t w2 = pack2<BF16>(pr[ch * 8 + 4], pr[ch * 8 + 5]);
-        const uint32_t w3 = pack2<BF16>(pr[ch * 8 + 6], pr[ch * 8 + 7]);
-        *reinterpret_cast<uint4*>(ds_row + ((ch ^ (kl & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->ds_full);
-    }
-    // ---- dV epilogue: this thread's key row, 128 columns
-    bool have = ok && T > 0;
-    if (have) {
-      have = wait_bar(&bars->acc_done, 0, abort_flag, p.status);
-      have = __all_sync(0xffffffffu, have);
-      tc_fence_after();
-    }
-    uint16_t* dst = reinterpret_cast<uint16_t*>(p.dv) + (static_cast<long long>(bkv) * p.Sk + key) * kD;
-#pragma unroll 1
-    for (int c = 0; c < kD / 32; ++c) {
-      uint32_t w[32];
-      if (have) {
-        tmem_ld32(tmem + lane_off + kColDV + c * 32, w);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t w[32];
+        tmem_ld32(colY + hf * 32, w);
         tmem_wait_ld();
         reg_fence32(w);
-      } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = 0u;
-      }
-      if (key < p.Sk) {
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = st_d[hf * 8 + c4];  // broadcast read
+          const int cb = hf * 32 + 4 * c4;
+          x[cb + 0] *= __uint_as_float(w[4 * c4 + 0]) - d4.x;
+          x[cb + 1] *= __uint_as_float(w[4 * c4 + 1]) - d4.y;
+          x[cb + 2] *= __uint_as_float(w[4 * c4 + 2]) - d4.z;
+          x[cb + 3] *= __uint_as_float(w[4 * c4 + 3]) - d4.w;
+        }
         uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]), __uint_as_float(w[2 * i + 1]));
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        pack32<BF16>(x, hf * 32, pk);
+        tmem_st16(colY + hf * 16, pk);  // dS^T over dP^T columns already read
       }
-    }
-  } else {
-    // ================================================================ Q warpgroup
-    const int wq = warp - 4;
-    const int dl = wq * 32 + lane;  // column of dQ (= TMEM lane of dQ^T)
-    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    float* stage = reinterpret_cast<float*>(smem + kOffStage);
-    bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      int h, q0;
-      block_coords(t, h, q0);
-      ok = wait_bar(&bars->dq_full, t & 1, abort_flag, p.status);
-      ok = named_bar_and(1, 128, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t u[kBM];
-      tmem_ld32(tmem + lane_off + kColDQ, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-      tmem_ld32(tmem + lane_off + kColDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-      tmem_wait_ld();
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bars->dq_free);
-      // the previous reduce must have finished reading the staging tile
-      if (dl == 0) bulk_wait_group_read0();
-      named_bar_sync(1, 128);
-#pragma unroll
-      for (int c = 0; c < kBM; ++c) stage[c * kD + dl] = __uint_as_float(u[c]) * p.scale;
-      fence_proxy_async_smem();
-      named_bar_sync(1, 128);
-      if (dl == 0) {
-        const int rows = min(kBM, p.Sq - q0);
-        float* dst = p.dq_acc + ((static_cast<long long>(b) * p.H + h) * p.Sq + q0) * kD;
-        bulk_reduce_add_f32(dst, stage, static_cast<uint32_t>(rows) * kD * 4u);
-        bulk_commit_group();
-      }
+      mbar_arrive(&bars->ds_full);
     }
-    if (dl == 0) bulk_wait_group0();
-    // ---- dK epilogue: key row = TMEM lane, scaled by tau
-    const int kl = dl;
-    const int key = k0 + kl;
+    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (x tau)
     bool have = ok && T > 0;
     if (have) {
       have = wait_bar(&bars->acc_done, 0, abort_flag, p.status);
       have = __all_sync(0xffffffffu, have);
       tc_fence_after();
     }
-    uint16_t* dst = reinterpret_cast<uint16_t*>(p.dk) + (static_cast<long long>(bkv) * p.Sk + key) * kD;
+    const float mul = wg ? p.scale : 1.f;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(wg ? p.dk : p.dv) +
+                    (static_cast<long long>(bkv) * p.Sk + key) * kD;
 #pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       uint32_t w[32];
       if (have) {
-        tmem_ld32(tmem + lane_off + kColDK + c * 32, w);
+        tmem_ld32(tmem + lane_off + (wg ? kColDK : kColDV) + c * 32, w);
         tmem_wait_ld();
         reg_fence32(w);
       } else {
@@ -555,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * p.scale, __uint_as_float(w[2 * i + 1]) * p.scale);
+          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
@@ -570,21 +476,321 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
-// D[row] = sum_t dO[row,t] * O[row,t] (fp32) and dq_acc[row, :] = 0.
-// 16 threads per row, 8 elements (16 bytes) each.
+// =========================================================================
+// Row owner: dQ.
+// =========================================================================
+namespace row {
+constexpr int kStages = 3;                 // K/V stages
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kOffKV = 0;                  // stage s: K at s*64 KiB, V 32 KiB after it
+constexpr int kOffBars = kOffKV + kStages * kStageBytes;
+constexpr int kSmemBytes = 1024 + kOffBars + 256;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kColDQ = 0, kColS = 128, kColP = 256, kColQ = 384, kColDO = 448;
+
+struct __align__(8) Bars {
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t qo_ready;
+  uint64_t s_full, s_free;
+  uint64_t dp_full, ds_full;
+  uint64_t dq_done;
+  uint64_t acc_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+}  // namespace row
+
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                  const BwdParams p) {
+  using namespace row;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+  volatile int* abort_flag = &bars->abort_flag;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- work unit: (batch * H + head, query block).  Groups of p.head_group
+  // heads (their K/V stay in L2); inside a group the query blocks descend
+  // (causal: the blocks with the most key tiles first) and heads vary
+  // fastest (query heads of one KV head run side by side).
+  const int BH = p.B * p.H;
+  const int group = blockIdx.x / (p.head_group * p.n_qtiles);
+  const int heads_here = min(p.head_group, BH - group * p.head_group);
+  const int r_in = blockIdx.x - group * p.head_group * p.n_qtiles;
+  const int bh = group * p.head_group + r_in % heads_here;
+  const int it = p.n_qtiles - 1 - r_in / heads_here;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int kvh = h / p.g;
+  const int q0 = it * kT;
+  int n = p.n_ktiles;  // key tiles this block visits
+  if (CAUSAL) {
+    const int lim = min(q0 + kT - 1, p.Sq - 1) + p.delta;  // largest visible key of the block
+    n = lim < 0 ? 0 : min(n, lim / kT + 1);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->kv_full[s], 1);
+      mbar_init(&bars->kv_empty[s], 1);
+    }
+    mbar_init(&bars->qo_ready, 256);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 256);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->dq_done, 1);
+    mbar_init(&bars->acc_done, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp >= kLoadWarp) {
+    regs_dec<kRegsCtl>();
+    if (warp == kLoadWarp) {
+      // ============================================================== loader
+      if (lane == 0 && n > 0) {
+        const uint64_t keep = policy_evict_last();  // K/V: re-read by every query block
+        int issued = 0;
+        for (int j = 0; j < n; ++j) {
+          const int s = j % kStages;
+          if (!wait_bar(&bars->kv_empty[s], ((j / kStages) & 1) ^ 1, abort_flag, p.status)) break;
+          uint8_t* dst = smem + kOffKV + s * kStageBytes;
+          mbar_arrive_expect_tx(&bars->kv_full[s], 2 * kTileBytes);
+          for (int cb = 0; cb < 2; ++cb) {
+            tma_load_3d(dst + cb * kBlock, &tmap_k, &bars->kv_full[s], cb * 64, j * kT, b * p.Hkv + kvh, keep);
+            tma_load_3d(dst + kTileBytes + cb * kBlock, &tmap_v, &bars->kv_full[s], cb * 64, j * kT,
+                        b * p.Hkv + kvh, keep);
+          }
+          issued = j + 1;
+        }
+        int dummy = 0;
+        volatile int* no_abort = reinterpret_cast<volatile int*>(&dummy);
+        for (int j = max(0, issued - kStages); j < issued; ++j)
+          bounded_wait(&bars->kv_full[j % kStages], (j / kStages) & 1, no_abort, p.status, kStatusTimeoutDrain);
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // ============================================================== MMA issuer
+      if (lane == 0 && n > 0) {
+        constexpr uint32_t kIdK = idesc_f16(BF16, false, false, 128, 128);  // S, dP (B K-major)
+        constexpr uint32_t kIdMN = idesc_f16(BF16, false, true, 128, 128);  // dQ (B MN-major)
+        const uint32_t aKV0 = smem_u32(smem + kOffKV);
+        // A from tensor memory: Q / dO rows hold d along 64 packed columns, a
+        // K-step of 16 elements = 8 columns.
+        auto issue_scores = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base) {
+          const uint64_t bd = smem_desc_sw128(b_base, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_ts(tmem + d_col, tmem + a_col + kk * 8, bd + kstep_kmajor(kk), kIdK, kk > 0 ? 1u : 0u);
+        };
+        // dS holds keys 0-63 in columns [0,32) of its region, 64-127 in [64,96).
+        auto issue_dq = [&](uint32_t b_base, bool accumulate) {
+          const uint64_t bd = smem_desc_sw128(b_base, kBlock, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_f16_ts(tmem + kColDQ, tmem + kColP + (kk / 4) * 64 + (kk % 4) * 8, bd + kstep_mnmajor(kk), kIdMN,
+                       (accumulate || kk > 0) ? 1u : 0u);
+        };
+        bool ok = wait_bar(&bars->qo_ready, 0, abort_flag, p.status) &&
+                  wait_bar(&bars->kv_full[0], 0, abort_flag, p.status);
+        if (ok) {
+          tc_fence_after();
+          issue_scores(kColS, kColQ, aKV0);
+          mma_commit(&bars->s_full);
+          issue_scores(kColP, kColDO, aKV0 + kTileBytes);
+          mma_commit(&bars->dp_full);
+        }
+        for (int j = 0; ok && j < n; ++j) {
+          const int s = j % kStages;
+          const uint32_t ph = j & 1;
+          if (j + 1 < n) {
+            // S(j+1) once both warpgroups hold S(j) in registers
+            const int s1 = (j + 1) % kStages;
+            if (!(ok = wait_bar(&bars->kv_full[s1], ((j + 1) / kStages) & 1, abort_flag, p.status))) break;
+            if (!(ok = wait_bar(&bars->s_free, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_scores(kColS, kColQ, aKV0 + s1 * kStageBytes);
+            mma_commit(&bars->s_full);
+          }
+          // dQ += dS(j) K_j
+          if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
+          tc_fence_after();
+          issue_dq(aKV0 + s * kStageBytes, j > 0);
+          mma_commit(&bars->dq_done);
+          mma_commit(&bars->kv_empty[s]);
+          if (j + 1 < n) {
+            // dP(j+1) over dS(j) once the dQ product has read it
+            if (!(ok = wait_bar(&bars->dq_done, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_scores(kColP, kColDO, aKV0 + ((j + 1) % kStages) * kStageBytes + kTileBytes);
+            mma_commit(&bars->dp_full);
+          }
+        }
+        mma_commit(&bars->acc_done);
+        int dummy = 0;
+        bounded_wait(&bars->acc_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status,
+                     kStatusTimeoutDrain);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ================================================================ softmax warpgroups
+    regs_inc<kRegsCompute>();
+    const int wg = warp / 4;                // keys [64 wg, 64 wg + 64) of a tile
+    const int rl = (warp % 4) * 32 + lane;  // query row within the block (= TMEM lane)
+    const int q_row = q0 + rl;
+    const bool row_ok = q_row < p.Sq;
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const long long grow = (static_cast<long long>(b) * p.H + h) * p.Sq + (row_ok ? q_row : 0);
+    // The row's Q (warpgroup 0) or dO (warpgroup 1) into tensor memory: the
+    // 16-bit pairs in memory are already the packed column words.
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(wg ? p.dout : p.q) + grow * kD);
+      const uint32_t colA = tmem + lane_off + (wg ? kColDO : kColQ);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = row_ok ? src[half * 8 + i] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * i] = v.x, w[4 * i + 1] = v.y, w[4 * i + 2] = v.z, w[4 * i + 3] = v.w;
+        }
+        tmem_st32(colA + half * 32, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->qo_ready);
+    }
+    float l2 = INFINITY, Dr = 0.f;  // rows past Sq / with no visible key: P = 0
+    if (row_ok) {
+      const float lse = p.lse[grow];
+      if (lse != -INFINITY) l2 = lse * kLog2e;
+      Dr = p.Dvec[grow];
+    }
+    const float lam = p.scale_log2;
+    const uint32_t colS = tmem + lane_off + kColS + wg * 64;
+    const uint32_t colP = tmem + lane_off + kColP + wg * 64;
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      const uint32_t ph = j & 1;
+      const int kb = j * kT + wg * 64;  // key of this warpgroup's first column
+      ok = wait_bar(&bars->s_full, ph, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[64];
+      tmem_ld32(colS, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(colS + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_wait_ld();
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tc_fence_before();
+      mbar_arrive(&bars->s_free);
+      // P = 2^(lambda s - LSE log2 e); masked: keys past Sk and (causal)
+      // keys later than q_row + delta, i.e. columns c > last_c.
+      const int last_vis = CAUSAL ? min(p.Sk - 1, q_row + p.delta) : p.Sk - 1;
+      const int last_c = last_vis - kb;
+      const bool need_mask = last_c < 63;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float e = ex2_approx(fmaf(x[c], lam, -l2));
+        if (need_mask && c > last_c) e = 0.f;
+        x[c] = e;
+      }
+      ok = wait_bar(&bars->dp_full, ph, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t w[32];
+        tmem_ld32(colP + hf * 32, w);
+        tmem_wait_ld();
+        reg_fence32(w);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[hf * 32 + i] *= __uint_as_float(w[i]) - Dr;
+        uint32_t pk[16];
+        pack32<BF16>(x, hf * 32, pk);
+        tmem_st16(colP + hf * 16, pk);  // dS over dP columns already read
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->ds_full);
+    }
+    // ---- epilogue: dQ row (x tau); warpgroup wg writes columns [64 wg, 64 wg + 64)
+    bool have = ok && n > 0;
+    if (have) {
+      have = wait_bar(&bars->acc_done, 0, abort_flag, p.status);
+      have = __all_sync(0xffffffffu, have);
+      tc_fence_after();
+    }
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) + grow * kD + wg * 64;
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      uint32_t w[32];
+      if (have) {
+        tmem_ld32(tmem + lane_off + kColDQ + wg * 64 + c * 32, w);
+        tmem_wait_ld();
+        reg_fence32(w);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = 0u;
+      }
+      if (row_ok) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * p.scale, __uint_as_float(w[2 * i + 1]) * p.scale);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+}
+
+// D[row] = sum_t dO[row,t] * O[row,t] (fp32); 16 threads per row, 8
+// elements (16 bytes) each.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __restrict__ o,
                                                              const uint16_t* __restrict__ dout,
-                                                             float* __restrict__ Dvec,
-                                                             float* __restrict__ dq_acc, long long n_rows) {
+                                                             float* __restrict__ Dvec, long long n_rows) {
   constexpr int kTpr = D / 8;  // threads per row
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long row = tid / kTpr;
+  const long long r = tid / kTpr;
   const int part = static_cast<int>(tid % kTpr);
   float acc = 0.f;
-  if (row < n_rows) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
-    const uint4 c = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
+  if (r < n_rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + r * D + part * 8);
+    const uint4 c = *reinterpret_cast<const uint4*>(dout + r * D + part * 8);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -600,54 +806,49 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
       acc = fmaf(a0, c0, acc);
       acc = fmaf(a1, c1, acc);
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + row * D + part * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int off = kTpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (row < n_rows && part == 0) Dvec[row] = acc;
+  if (r < n_rows && part == 0) Dvec[r] = acc;
 }
 
-// dq[i] = dtype(dq_acc[i]), 8 elements per thread.
-template <bool BF16>
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float* __restrict__ dq_acc,
-                                                             uint16_t* __restrict__ dq, long long n8) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4*>(dq_acc)[2 * i];
-  const float4 c = reinterpret_cast<const float4*>(dq_acc)[2 * i + 1];
-  reinterpret_cast<uint4*>(dq)[i] =
-      make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(c.x, c.y), pack2<BF16>(c.z, c.w));
+// Heads per L2 scheduling group: about 48 MB of the operands a group re-reads.
+int head_group_for(long long per_head_bytes, long long heads) {
+  long long hg = (48LL << 20) / (per_head_bytes > 0 ? per_head_bytes : 1);
+  if (hg < 1) hg = 1;
+  return static_cast<int>(hg < heads ? hg : heads);
 }
 
 template <bool BF16, bool CAUSAL>
 int launch_bwd_t(const BackwardArgs& a) {
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_3d(&tq, a.q, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
-      !make_tmap_3d(&tdo, a.dout, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
-      !make_tmap_3d(&tk, a.k, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN) ||
-      !make_tmap_3d(&tv, a.v, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN))
+  if (!make_tmap_3d(&tq, a.q, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tdo, a.dout, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tk, a.k, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
+      !make_tmap_3d(&tv, a.v, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
     return -1;
   const long long n_rows = static_cast<long long>(a.B) * a.H * a.Sq;
   {
-    const long long threads = n_rows * (kD / 8);
-    const long long blocks = (threads + 255) / 256;
+    const long long blocks = (n_rows * (kD / 8) + 255) / 256;
     if (blocks > 0x7FFFFFFFLL) return -1;
     bwd_preprocess_kernel<kD, BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
-        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.Dvec, a.dq_acc, n_rows);
+        static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.Dvec, n_rows);
   }
-  auto kern = bwd_main_kernel<BF16, CAUSAL>;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             col::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_dq_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             row::kSmemBytes) != cudaSuccess)
       return -1;
     attr_set = true;
   }
   BwdParams p;
   p.lse = a.lse;
   p.Dvec = a.Dvec;
-  p.dq_acc = a.dq_acc;
+  p.q = a.q;
+  p.dout = a.dout;
+  p.dq = a.dq;
   p.dk = a.dk;
   p.dv = a.dv;
   p.B = a.B;
@@ -656,29 +857,25 @@ int launch_bwd_t(const BackwardArgs& a) {
   p.Sq = a.Sq;
   p.Sk = a.Sk;
   p.g = a.H / a.Hkv;
-  p.n_ktiles = (a.Sk + kBN - 1) / kBN;
-  {
-    // KV heads per scheduling group: about 48 MB of Q, dO (16-bit) and the
-    // fp32 dQ accumulator of their query heads in flight (L2 is 129 MB).
-    const long long per_kv = static_cast<long long>(p.g) * a.Sq * kD * (2 + 2 + 4);
-    long long hg = (48LL << 20) / (per_kv > 0 ? per_kv : 1);
-    if (hg < 1) hg = 1;
-    const long long BHkv = static_cast<long long>(a.B) * a.Hkv;
-    p.head_group = static_cast<int>(hg < BHkv ? hg : BHkv);
-  }
+  p.n_ktiles = (a.Sk + kT - 1) / kT;
+  p.n_qtiles = (a.Sq + kT - 1) / kT;
   p.delta = a.Sk - a.Sq;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.status = a.status;
-  const long long grid = static_cast<long long>(a.B) * a.Hkv * p.n_ktiles;
-  if (grid > 0x7FFFFFFFLL) return -1;
-  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tdo, p);
-  {
-    const long long n8 = n_rows * kD / 8;
-    const long long blocks = (n8 + 255) / 256;
-    bwd_dq_convert_kernel<BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
-        a.dq_acc, static_cast<uint16_t*>(a.dq), n8);
-  }
+  // column owner: a KV head's group re-reads its query heads' Q and dO
+  p.head_group = head_group_for(static_cast<long long>(p.g) * a.Sq * kD * 4,
+                                static_cast<long long>(a.B) * a.Hkv);
+  const long long grid_a = static_cast<long long>(a.B) * a.Hkv * p.n_ktiles;
+  if (grid_a > 0x7FFFFFFFLL) return -1;
+  bwd_dkdv_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid_a), kThreads, col::kSmemBytes, a.stream>>>(
+      tq, tk, tv, tdo, p);
+  // row owner: a query head re-reads its KV head's K and V
+  BwdParams pr = p;
+  pr.head_group = head_group_for(static_cast<long long>(a.Sk) * kD * 4, static_cast<long long>(a.B) * a.H);
+  const long long grid_b = static_cast<long long>(a.B) * a.H * p.n_qtiles;
+  if (grid_b > 0x7FFFFFFFLL) return -1;
+  bwd_dq_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid_b), kThreads, row::kSmemBytes, a.stream>>>(tk, tv, pr);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

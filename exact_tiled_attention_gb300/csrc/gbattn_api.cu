@@ -178,14 +178,10 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
   return launch_decode(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
-static size_t bwd_d_bytes(int B, int H, int Sq) {
-  // row scalars D, rounded up to 256 bytes so the accumulator stays aligned
-  return ((static_cast<size_t>(B) * H * Sq * sizeof(float)) + 255) & ~static_cast<size_t>(255);
-}
-
 size_t attn_bwd_workspace_bytes(int B, int H, int Sq, int d) {
   if (B < 1 || H < 1 || Sq < 1 || d < 1) return 0;
-  return bwd_d_bytes(B, H, Sq) + static_cast<size_t>(B) * H * Sq * d * sizeof(float);
+  // the fp32 row scalars D, rounded up to 256 bytes
+  return ((static_cast<size_t>(B) * H * Sq * sizeof(float)) + 255) & ~static_cast<size_t>(255);
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -225,7 +221,6 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.scale = scale;
   a.causal = causal ? 1 : 0;
   a.Dvec = static_cast<float*>(workspace);
-  a.dq_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + bwd_d_bytes(B, H, Sq));
   a.bf16 = dtype == GBATTN_BF16;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = status;

@@ -55,8 +55,7 @@ struct BackwardArgs {
   int B, H, Hkv, Sq, Sk, d;
   float scale;
   int causal;
-  float* Dvec;    // workspace: [B*H*Sq] fp32
-  float* dq_acc;  // workspace: [B*H*Sq*d] fp32
+  float* Dvec;    // workspace: [B*H*Sq] fp32 row scalars D
   bool bf16;
   cudaStream_t stream;
   int* status;

@@ -135,11 +135,10 @@ int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
 
 /*
  * attn_bwd_workspace_bytes -- bytes of device workspace attn_bwd needs: the
- * fp32 row scalars D [B, H, Sq] (rounded up to 256 bytes) followed by the fp32
- * dQ accumulator [B, H, Sq, d].  For B=1, H=32, Sq=4096, d=128 this is the
- * 0.5 MiB + 64 MiB of the scratch ledger in M4.4 0x06.1J (the expanded
- * per-query-head dK/dV buffers of that ledger are not needed here).
- * Returns 0 for invalid sizes.
+ * fp32 row scalars D [B, H, Sq] (rounded up to 256 bytes).  For B=1, H=32,
+ * Sq=4096 this is the 0.5 MiB D entry of the scratch ledger in M4.4 0x06.1J;
+ * the ledger's fp32 dQ accumulator and expanded per-query-head dK/dV buffers
+ * are not needed (see attn_bwd).  Returns 0 for invalid sizes.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int Sq, int d);
 
@@ -160,13 +159,14 @@ size_t attn_bwd_workspace_bytes(int B, int H, int Sq, int d);
  * Definition (M4.4 0x06.1A): with P_ij = exp(scale q_i.k_j - LSE_i) over the
  * visible keys, dP = dO V^T, D_i = dO_i . O_i, dS = P o (dP - D),
  * dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.  Three kernels run in
- * stream order (0x06.1D): D and a zeroed fp32 dQ accumulator; one CTA per
- * (128-key tile, batch, KV head) that keeps the tile's dK, dV in tensor
- * memory over every visible query block of every query head in the group
- * (0x06.1B column owner; the GQA sum of 0x06.1H happens in the accumulator)
- * and adds each block's dQ into the accumulator with asynchronous fp32
- * reduce-adds (0x06.1F: atomic, unordered -- dQ is not bitwise repeatable);
- * then the conversion of dQ to dtype.
+ * stream order: D; one CTA per (128-key tile, batch, KV head) that keeps the
+ * tile's dK, dV in tensor memory over every visible query block of every
+ * query head in the group (the column owner of 0x06.1B; the GQA sum of
+ * 0x06.1H happens in the accumulator); one CTA per (128-row query block,
+ * batch, query head) that keeps the block's dQ in tensor memory over every
+ * visible key tile (the row owner of 0x06.1I).  Each owner recomputes the
+ * scores it needs, so every output element has a single writer and a fixed
+ * summation order: results are bitwise repeatable (no atomics, 0x06.1F).
  *
  * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM (d must be 128), EDTYPE,
  * EPOINTER (every pointer required; lse 4-byte aligned), EWORKSPACE,

@@ -139,12 +139,13 @@ def _bwd(lib, **kw):
 
 
 def test_bwd_workspace_matches_page_ledger(lib, golden):
-    """The backward workspace is the fp32 dQ accumulator plus the row scalars
-    D: at the ledger coordinate of M4.4 0x06.1J that is 64 MiB + 0.5 MiB."""
+    """The backward workspace is the fp32 row scalars D alone: at the ledger
+    coordinate of M4.4 0x06.1J that is the ledger's 0.5 MiB D entry (the
+    ledger's dQaccum and expanded dK/dV have no counterpart here)."""
     g = golden("bwd_scratch_ledger.json")
     c = g["coordinate"]
     mib = 1 << 20
-    want = (g["objects_mib"]["dQaccum"] + g["objects_mib"]["D"]) * mib
+    want = g["objects_mib"]["D"] * mib
     assert lib.attn_bwd_workspace_bytes(c["B"], c["Hq"], c["Sq"], c["d"]) == want
     assert lib.attn_bwd_workspace_bytes(0, 1, 1, 128) == 0
 

@@ -92,3 +92,16 @@ def test_bwd_workload_sampled_heads(name, kv_ids):
         assert_grad_close(dq[b, kvh * g:(kvh + 1) * g], rq[r], f"{name} dq kv{kid}")
         assert_grad_close(dk[b, kvh], rk[r], f"{name} dk kv{kid}")
         assert_grad_close(dv[b, kvh], rv[r], f"{name} dv kv{kid}")
+
+
+def test_bwd_bitwise_repeatable():
+    """Every gradient element has one writer and a fixed summation order, so
+    two calls give identical bits."""
+    q, k, v = make_prefill(1, 4, 2, 700, 700, 128, torch.bfloat16, 51, device="cuda")
+    do = _dout(q.shape, torch.bfloat16, 52)
+    o, lse = attn_fwd(q, k, v, causal=True)
+    a = attn_bwd(q, k, v, o, lse, do, causal=True)
+    b = attn_bwd(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
