@@ -41,10 +41,11 @@
 // tile's 128 keys:
 //     S    = Q K_j^T       A = Q (tensor memory),    B = K_j (smem, K-major)
 //     dP   = dO V_j^T      A = dO (tensor memory),   B = V_j (smem, K-major)
-//     dQ  += dS K_j        A = dS (tensor memory),   B = K_j (smem, MN-major)
-//   Q and dO are written to tensor memory once per CTA; dS (input dtype)
-//   overwrites the fp32 dP it came from.
-//   TMEM: dQ [0,128), S [128,256), dP/dS [256,384), Q [384,448), dO [448,512).
+//     dQ  += dS K_j        A = dS (smem, K-major),   B = K_j (smem, MN-major)
+//   Q and dO are written to tensor memory once per CTA; dS (input dtype) is
+//   staged in shared memory, so dP(j+1) can be issued as soon as dP(j) is in
+//   registers, while dS(j) is still being formed.
+//   TMEM: dQ [0,128), S [128,256), dP [256,384), Q [384,448), dO [448,512).
 //
 // A 128 x 128 x 16 MMA with both operands in shared memory is bound by the
 // shared-memory operand reads (two 4 KiB operands per ~70 cycles, measured);
@@ -483,7 +484,8 @@ namespace row {
 constexpr int kStages = 3;                 // K/V stages
 constexpr int kStageBytes = 2 * kTileBytes;
 constexpr int kOffKV = 0;                  // stage s: K at s*64 KiB, V 32 KiB after it
-constexpr int kOffBars = kOffKV + kStages * kStageBytes;
+constexpr int kOffDS = kOffKV + kStages * kStageBytes;  // dS, K-major A of the dQ product
+constexpr int kOffBars = kOffDS + kTileBytes;
 constexpr int kSmemBytes = 1024 + kOffBars + 256;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kColDQ = 0, kColS = 128, kColP = 256, kColQ = 384, kColDO = 448;
@@ -493,8 +495,8 @@ struct __align__(8) Bars {
   uint64_t kv_empty[kStages];
   uint64_t qo_ready;
   uint64_t s_full, s_free;
-  uint64_t dp_full, ds_full;
-  uint64_t dq_done;
+  uint64_t dp_full, dp_free;
+  uint64_t ds_full, ds_free;
   uint64_t acc_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -544,8 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 256);
     mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 256);
     mbar_init(&bars->ds_full, 256);
-    mbar_init(&bars->dq_done, 1);
+    mbar_init(&bars->ds_free, 1);
     mbar_init(&bars->acc_done, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -602,12 +605,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kD / 16; ++kk)
             mma_f16_ts(tmem + d_col, tmem + a_col + kk * 8, bd + kstep_kmajor(kk), kIdK, kk > 0 ? 1u : 0u);
         };
-        // dS holds keys 0-63 in columns [0,32) of its region, 64-127 in [64,96).
+        const uint64_t dDS_A = smem_desc_sw128(smem_u32(smem + kOffDS), 16, 1024);
         auto issue_dq = [&](uint32_t b_base, bool accumulate) {
           const uint64_t bd = smem_desc_sw128(b_base, kBlock, 1024);
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_f16_ts(tmem + kColDQ, tmem + kColP + (kk / 4) * 64 + (kk % 4) * 8, bd + kstep_mnmajor(kk), kIdMN,
+            mma_f16_ss(tmem + kColDQ, dDS_A + kstep_kmajor(kk), bd + kstep_mnmajor(kk), kIdMN,
                        (accumulate || kk > 0) ? 1u : 0u);
         };
         bool ok = wait_bar(&bars->qo_ready, 0, abort_flag, p.status) &&
@@ -623,27 +626,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = j % kStages;
           const uint32_t ph = j & 1;
           if (j + 1 < n) {
-            // S(j+1) once both warpgroups hold S(j) in registers
             const int s1 = (j + 1) % kStages;
             if (!(ok = wait_bar(&bars->kv_full[s1], ((j + 1) / kStages) & 1, abort_flag, p.status))) break;
+            // S(j+1) once both warpgroups hold S(j) in registers
             if (!(ok = wait_bar(&bars->s_free, ph, abort_flag, p.status))) break;
             tc_fence_after();
             issue_scores(kColS, kColQ, aKV0 + s1 * kStageBytes);
             mma_commit(&bars->s_full);
+            // dP(j+1) once both warpgroups hold dP(j) in registers
+            if (!(ok = wait_bar(&bars->dp_free, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_scores(kColP, kColDO, aKV0 + s1 * kStageBytes + kTileBytes);
+            mma_commit(&bars->dp_full);
           }
           // dQ += dS(j) K_j
           if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
           tc_fence_after();
           issue_dq(aKV0 + s * kStageBytes, j > 0);
-          mma_commit(&bars->dq_done);
+          mma_commit(&bars->ds_free);
           mma_commit(&bars->kv_empty[s]);
-          if (j + 1 < n) {
-            // dP(j+1) over dS(j) once the dQ product has read it
-            if (!(ok = wait_bar(&bars->dq_done, ph, abort_flag, p.status))) break;
-            tc_fence_after();
-            issue_scores(kColP, kColDO, aKV0 + ((j + 1) % kStages) * kStageBytes + kTileBytes);
-            mma_commit(&bars->dp_full);
-          }
         }
         mma_commit(&bars->acc_done);
         int dummy = 0;
@@ -689,6 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float lam = p.scale_log2;
     const uint32_t colS = tmem + lane_off + kColS + wg * 64;
     const uint32_t colP = tmem + lane_off + kColP + wg * 64;
+    uint8_t* ds_row = smem + kOffDS + wg * kBlock + rl * 128;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const uint32_t ph = j & 1;
@@ -730,14 +732,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(colP + hf * 32, w);
         tmem_wait_ld();
         reg_fence32(w);
+        if (hf == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars->dp_free);  // dP(j+1) may now overwrite the columns
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) x[hf * 32 + i] *= __uint_as_float(w[i]) - Dr;
+      }
+      // dS row into shared memory (column block wg, row rl; 16-byte chunk c
+      // at chunk c ^ (rl % 8)) once the dQ product of tile j-1 has read it.
+      if (j > 0) {
+        ok = wait_bar(&bars->ds_free, (j - 1) & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
         uint32_t pk[16];
         pack32<BF16>(x, hf * 32, pk);
-        tmem_st16(colP + hf * 16, pk);  // dS over dP columns already read
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const int cc = hf * 4 + ch;
+          *reinterpret_cast<uint4*>(ds_row + ((cc ^ (rl & 7)) << 4)) =
+              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+        }
       }
-      tmem_wait_st();
-      tc_fence_before();
+      fence_proxy_async_smem();
       mbar_arrive(&bars->ds_full);
     }
     // ---- epilogue: dQ row (x tau); warpgroup wg writes columns [64 wg, 64 wg + 64)
