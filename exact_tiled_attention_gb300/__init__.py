@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     error_string,
     gbattn_causal_tile_counts,
     gbattn_device_status,
+    gbattn_exp2_paths,
     gbattn_version,
     load_library,
 )

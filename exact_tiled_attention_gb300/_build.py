@@ -2,6 +2,10 @@
 extension machinery): each .cu compiles in parallel, then one link step.
 
     python -m exact_tiled_attention_gb300._build [--force] [--verbose]
+
+Build option (environment): GBATTN_EX2_EMU_EVERY=E evaluates every E-th pair
+of softmax exponentials with the FMA-pipe polynomial instead of the MUFU unit
+(default 0 = none; the library is rebuilt when the setting changes).
 """
 from __future__ import annotations
 
@@ -45,13 +49,21 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+def _options() -> list[str]:
+    emu = int(os.environ.get("GBATTN_EX2_EMU_EVERY", "0") or 0)
+    return [f"-DGBATTN_EX2_EMU_EVERY={emu}"]
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     deps = _deps()
-    if not force and not _stale(LIB, deps):
+    stamp = os.path.join(BUILD, "options.txt")
+    opts = _options()
+    old = open(stamp).read() if os.path.exists(stamp) else ""
+    if not force and not _stale(LIB, deps) and old == " ".join(opts):
         return LIB
     cc = nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    extra = (["-Xptxas", "-v"] if ptxas_verbose else []) + opts
 
     def compile_one(src: str):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
@@ -75,6 +87,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc link failed")
     os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(" ".join(opts))
     return LIB
 
 

@@ -28,7 +28,7 @@ ERRORS = {
 }
 EXPORTS = ("attn_fwd", "attn_decode_workspace_bytes", "attn_decode_splitkv",
            "attn_decode_splitkv_noalloc", "attn_decode_noalloc_scratch_bytes",
-           "attn_bwd_workspace_bytes", "attn_bwd",
+           "attn_bwd_workspace_bytes", "attn_bwd", "gbattn_exp2_paths",
            "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_error_string",
            "gbattn_version")
 
@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
                                  sz, ci, vp]
         lib.attn_bwd.restype = ci
+        lib.gbattn_exp2_paths.argtypes = [vp, vp, vp, ctypes.c_longlong, vp]
+        lib.gbattn_exp2_paths.restype = ci
         lib.gbattn_causal_tile_counts.argtypes = [ci, ci, ci, ci, ll_p, ll_p, ll_p, ll_p, ll_p]
         lib.gbattn_causal_tile_counts.restype = ci
         lib.gbattn_device_status.argtypes = []
@@ -273,6 +275,19 @@ def gbattn_causal_tile_counts(Sq: int, Sk: int, Br: int, Bc: int) -> dict:
         raise GbattnError(rc, "gbattn_causal_tile_counts")
     keys = ("full", "partial", "skipped", "allowed_cells", "visited_cells")
     return {k: v.value for k, v in zip(keys, vals)}
+
+
+def gbattn_exp2_paths(x, stream=None):
+    """Diagnostic: (software polynomial 2^x, hardware ex2.approx 2^x) for a
+    contiguous fp32 CUDA tensor x with an even number of elements."""
+    if not (isinstance(x, torch.Tensor) and x.is_cuda and x.dtype == torch.float32 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous fp32 CUDA tensor")
+    y_poly, y_hw = torch.empty_like(x), torch.empty_like(x)
+    rc = load_library().gbattn_exp2_paths(x.data_ptr(), y_poly.data_ptr(), y_hw.data_ptr(), x.numel(),
+                                          _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "gbattn_exp2_paths")
+    return y_poly, y_hw
 
 
 def gbattn_device_status() -> int:

@@ -388,13 +388,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
         const float4 l4 = st_l[c4];  // broadcast read
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = 4 * c4 + i;
-          float e = ex2_approx(fmaf(x[c], lam, -lv[i]));
-          if (need_mask && c < first_c) e = 0.f;
-          x[c] = e;
+        for (int i = 0; i < 2; ++i) {
+          const int c = 4 * c4 + 2 * i;
+          const float2 e = ex2_pair(make_float2(fmaf(x[c], lam, -(i ? l4.z : l4.x)),
+                                                fmaf(x[c + 1], lam, -(i ? l4.w : l4.y))),
+                                    c / 2);
+          x[c] = (need_mask && c < first_c) ? 0.f : e.x;
+          x[c + 1] = (need_mask && c + 1 < first_c) ? 0.f : e.y;
         }
       }
       {
@@ -715,10 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int last_c = last_vis - kb;
       const bool need_mask = last_c < 63;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float e = ex2_approx(fmaf(x[c], lam, -l2));
-        if (need_mask && c > last_c) e = 0.f;
-        x[c] = e;
+      for (int c = 0; c < 64; c += 2) {
+        const float2 e = ex2_pair(make_float2(fmaf(x[c], lam, -l2), fmaf(x[c + 1], lam, -l2)), c / 2);
+        x[c] = (need_mask && c > last_c) ? 0.f : e.x;
+        x[c + 1] = (need_mask && c + 1 > last_c) ? 0.f : e.y;
       }
       ok = wait_bar(&bars->dp_full, ph, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) {

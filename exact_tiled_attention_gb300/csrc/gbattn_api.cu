@@ -9,6 +9,7 @@
 
 #include "../../include/gbattn.h"
 #include "gbattn_internal.h"
+#include "gbattn_ptx.cuh"
 
 namespace gbattn {
 
@@ -91,6 +92,17 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, int d, int rows
           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Both exp2 paths of the kernels on n values: y_poly = ex2_poly3_x2 (FMA
+// pipe), y_hw = ex2.approx (MUFU).  n is even.
+__global__ void ex2_paths_kernel(const float* __restrict__ x, float* __restrict__ y_poly,
+                                 float* __restrict__ y_hw, long long n2) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n2) return;
+  const float2 v = reinterpret_cast<const float2*>(x)[i];
+  reinterpret_cast<float2*>(y_poly)[i] = ex2_poly3_x2(v);
+  reinterpret_cast<float2*>(y_hw)[i] = make_float2(ex2_approx(v.x), ex2_approx(v.y));
 }
 
 }  // namespace gbattn
@@ -262,6 +274,22 @@ int gbattn_causal_tile_counts(int Sq, int Sk, int Br, int Bc, long long* full, l
   if (allowed_cells) *allowed_cells = allowed;
   if (visited_cells) *visited_cells = visited;
   return GBATTN_OK;
+}
+
+int gbattn_exp2_paths(const float* x, float* y_poly, float* y_hw, long long n, void* stream) {
+  if (n < 0 || (n & 1)) return GBATTN_EBADSHAPE;
+  if (n == 0) return GBATTN_OK;
+  if (!x || !y_poly || !y_hw || (reinterpret_cast<uintptr_t>(x) & 7u) ||
+      (reinterpret_cast<uintptr_t>(y_poly) & 7u) || (reinterpret_cast<uintptr_t>(y_hw) & 7u))
+    return GBATTN_EPOINTER;
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  const long long n2 = n / 2, blocks = (n2 + 255) / 256;
+  if (blocks > 0x7FFFFFFFLL) return GBATTN_EBADSHAPE;
+  ex2_paths_kernel<<<static_cast<unsigned>(blocks), 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y_poly, y_hw,
+                                                                                                 n2);
+  return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
 int gbattn_device_status(void) {

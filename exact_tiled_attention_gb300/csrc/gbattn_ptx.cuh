@@ -351,6 +351,48 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Software 2^x for two values on the FMA/ALU pipes instead of the MUFU unit
+// (M4.6 "FlashAttention-3/4 Hardware Pipelines" 0x09, software exp2):
+// range reduction 2^x = 2^n p(f) with n = floor(x), f = x - n in [0, 1), and
+// p the degree-3 polynomial with p(0) = 1 that minimises the maximum relative
+// error on [0, 1] (coefficients from exp2_poly_fit.py; 8.6e-5 in exact
+// arithmetic).  floor(x) comes from adding 1.5 * 2^23 with round-down, whose
+// low mantissa bits then hold n; 2^n is applied by adding n to the exponent
+// field of p(f).  Inputs are clamped to [-126, 127]: below -126 the result is
+// 2^-126 (a probability of ~1e-38 instead of 0).
+__device__ __forceinline__ float2 ex2_poly3_x2(float2 x) {
+  constexpr float kC1 = 6.951167864e-01f, kC2 = 2.276449912e-01f, kC3 = 7.706704199e-02f;
+  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: spacing 1 around it
+  x.x = fminf(fmaxf(x.x, -126.f), 127.f);
+  x.y = fminf(fmaxf(x.y, -126.f), 127.f);
+  const float tx = __fadd_rd(x.x, kMagic), ty = __fadd_rd(x.y, kMagic);
+  const float2 f = fadd2(x, make_float2(kMagic - tx, kMagic - ty));  // x - floor(x)
+  float2 q = ffma2(make_float2(kC3, kC3), f, make_float2(kC2, kC2));
+  q = ffma2(q, f, make_float2(kC1, kC1));
+  q = ffma2(q, f, make_float2(1.f, 1.f));
+  const uint32_t nx = __float_as_uint(tx) - __float_as_uint(kMagic);  // n, two's complement
+  const uint32_t ny = __float_as_uint(ty) - __float_as_uint(kMagic);
+  return make_float2(__uint_as_float(__float_as_uint(q.x) + (nx << 23)),
+                     __uint_as_float(__float_as_uint(q.y) + (ny << 23)));
+}
+
+// Share of the softmax exponentials the kernels evaluate with ex2_poly3_x2
+// instead of the MUFU unit: every GBATTN_EX2_EMU_EVERY-th pair of elements
+// (0 = none).  A build option; on GB300 (MUFU ex2 at 32 per clock per SM)
+// every non-zero setting measured slower for both the forward and the
+// backward, so the default is 0.
+#ifndef GBATTN_EX2_EMU_EVERY
+#define GBATTN_EX2_EMU_EVERY 0
+#endif
+constexpr int kEx2EmuEvery = GBATTN_EX2_EMU_EVERY;
+
+// 2^x for a pair of softmax arguments; pair index `pair` selects the path.
+__device__ __forceinline__ float2 ex2_pair(float2 t, int pair) {
+  if (kEx2EmuEvery > 0 && (pair % (kEx2EmuEvery > 0 ? kEx2EmuEvery : 1)) == kEx2EmuEvery - 1)
+    return ex2_poly3_x2(t);
+  return make_float2(ex2_approx(t.x), ex2_approx(t.y));
+}
+
 // Pack two fp32 values into one 32-bit word of two 16-bit values; `lo` goes
 // to bits 0-15 (the lower element index), `hi` to bits 16-31.  RN-even.
 template <bool BF16>

@@ -458,9 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int c = ch * 8 + 2 * i;
-          float2 t = ffma2(make_float2(s[c], s[c + 1]), lam2, nrs2);
-          t.x = ex2_approx(t.x);
-          t.y = ex2_approx(t.y);
+          const float2 t = ex2_pair(ffma2(make_float2(s[c], s[c + 1]), lam2, nrs2), ch * 4 + i);
           sum4[i] = fadd2(sum4[i], t);
           pk[i] = pack2<BF16>(t.x, t.y);
         }

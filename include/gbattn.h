@@ -222,6 +222,21 @@ int gbattn_causal_tile_counts(int Sq, int Sk, int Br, int Bc,
                               long long *allowed_cells, long long *visited_cells);
 
 /*
+ * gbattn_exp2_paths -- diagnostic: evaluates the two base-2 exponentials the
+ * kernels can use on n (even) device fp32 values x, writing
+ *   y_poly[i]: the FMA-pipe software path (range reduction 2^x = 2^n p(f),
+ *              degree-3 polynomial p on [0, 1), inputs clamped to
+ *              [-126, 127]) -- the software exp2 of M4.6 0x09;
+ *   y_hw[i]:   the hardware MUFU approximation (ex2.approx.ftz).
+ * All pointers are 8-byte aligned device pointers; work is enqueued on
+ * `stream`.  It exists so that tests can pin the software path's accuracy
+ * (M4.6 0x09 states a degree-3 maximum relative error near 9e-5); the method
+ * has no counterpart.  Errors: GBATTN_EBADSHAPE (n < 0 or odd),
+ * GBATTN_EPOINTER, GBATTN_EUNSUPPORTED, GBATTN_ELAUNCH.
+ */
+int gbattn_exp2_paths(const float *x, float *y_poly, float *y_hw, long long n, void *stream);
+
+/*
  * gbattn_device_status -- read and clear the library's device status word
  * (synchronises the current device).  Returns GBATTN_OK, or
  * GBATTN_EDEVICE_TIMEOUT if a kernel gave up a bounded wait since the last
