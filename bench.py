@@ -50,7 +50,8 @@ DECODE = WORKLOADS["decode_splitkv_bf16_b64_hq32_hkv8_sk32768_d128"]
 OTHER_PREFILL = [WORKLOADS["prefill_fp16_b1_h8_s4096_d64"],
                  WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"]]
 # Backward workloads (d = 128), measured in the default run under "backward".
-BACKWARD = [WORKLOADS["causal_bf16_b4_h16_s8192_d128"], WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"]]
+BACKWARD = [WORKLOADS["causal_bf16_b4_h16_s8192_d128"], WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"],
+            WORKLOADS["prefill_fp16_b1_h8_s4096_d64"]]
 PREFILL_METRIC = "attention fwd TFLOP/s (% BF16 tensor peak)"
 DECODE_METRIC = "decode HBM GB/s (% peak)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

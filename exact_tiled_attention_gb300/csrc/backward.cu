@@ -68,8 +68,7 @@
 namespace gbattn {
 namespace {
 
-constexpr int kD = 128;      // head dimension of these kernels
-constexpr int kT = 128;      // rows (keys or queries) per tile
+constexpr int kT = 128;      // rows (keys or queries) per tile; head dimension D = 64 or 128
 constexpr int kThreads = 384;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
@@ -77,8 +76,8 @@ constexpr int kRegsCompute = 184, kRegsCtl = 136;
 static_assert(2 * 128 * kRegsCompute + 128 * kRegsCtl <= kThreads * 168, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr int kTileBytes = kT * kD * 2;  // 32 KiB: 128 rows x 128 16-bit columns
-constexpr int kBlock = kT * 128;         // 16 KiB: 128 rows x one 128-byte column block
+constexpr int kBlock = kT * 128;         // 16 KiB: 128 rows x one 128-byte (64-element) column block
+constexpr int kDSBytes = kT * kT * 2;    // 32 KiB: a 128 x 128 16-bit dS tile
 
 struct BwdParams {
   const float* lse;   // [B,H,Sq] natural log
@@ -119,43 +118,47 @@ __device__ __forceinline__ void pack32(const float (&x)[64], int base, uint32_t 
 // =========================================================================
 // Column owner: dK, dV.
 // =========================================================================
-namespace col {
-constexpr int kStages = 2;
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kTileBytes;
-constexpr int kOffQ = kOffV + kTileBytes;                 // kStages tiles
-constexpr int kOffDO = kOffQ + kStages * kTileBytes;      // kStages tiles
-constexpr int kOffStats = kOffDO + kStages * kTileBytes;  // kStages x (128 lse2 + 128 D) fp32
-constexpr int kOffBars = kOffStats + kStages * 2 * kT * 4;
-constexpr int kSmemBytes = 1024 + kOffBars + 256;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kColDV = 0, kColDK = 128, kColX = 256, kColY = 384;
+template <int D>
+struct ColCfg {
+  static constexpr int kTileBytes = kT * D * 2;          // a 128-row tile of Q, dO, K or V
+  static constexpr int kStages = (D == 128) ? 2 : 4;     // Q/dO stages
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffQ = kOffV + kTileBytes;                 // kStages tiles
+  static constexpr int kOffDO = kOffQ + kStages * kTileBytes;      // kStages tiles
+  static constexpr int kOffStats = kOffDO + kStages * kTileBytes;  // kStages x (128 lse2 + 128 D) fp32
+  static constexpr int kOffBars = kOffStats + kStages * 2 * kT * 4;
+  static constexpr int kSmemBytes = 1024 + kOffBars + 256;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // TMEM: dV, dK (D columns each), S^T/P^T and dP^T/dS^T (128 each)
+  static constexpr uint32_t kColDV = 0, kColDK = D, kColX = 2 * D, kColY = 2 * D + 128;
 
-struct __align__(8) Bars {
-  uint64_t kv_full;
-  uint64_t qd_full[kStages];
-  uint64_t qd_empty[kStages];
-  uint64_t s_full, dp_full;
-  uint64_t p_full, ds_full;
-  uint64_t dv_done, dk_done;
-  uint64_t acc_done;
-  uint32_t tmem_base;
-  int abort_flag;
+  struct __align__(8) Bars {
+    uint64_t kv_full;
+    uint64_t qd_full[kStages];
+    uint64_t qd_empty[kStages];
+    uint64_t s_full, dp_full;
+    uint64_t p_full, ds_full;
+    uint64_t dv_done, dk_done;
+    uint64_t acc_done;
+    uint32_t tmem_base;
+    int abort_flag;
+  };
+  static_assert(sizeof(Bars) <= 256, "barrier block");
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
-}  // namespace col
 
-template <bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
                     const __grid_constant__ CUtensorMap tmap_do, const BwdParams p) {
-  using namespace col;
+  using C = ColCfg<D>;
+  using Bars = typename C::Bars;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
-  float* stats = reinterpret_cast<float*>(smem + kOffStats);  // [stage][lse2 128 | D 128]
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBars);
+  float* stats = reinterpret_cast<float*>(smem + C::kOffStats);  // [stage][lse2 128 | D 128]
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->kv_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->qd_full[s], 1 + 32);  // TMA arrive + 32 lanes' stat stores
       mbar_init(&bars->qd_empty[s], 1);
     }
@@ -226,25 +229,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t once = policy_evict_first();  // K/V: read by this CTA only
       const uint64_t reuse = policy_evict_last();  // Q/dO: re-read by every key tile
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars->kv_full, 2 * kTileBytes);
-        for (int cb = 0; cb < 2; ++cb) {
-          tma_load_3d(smem + kOffK + cb * kBlock, &tmap_k, &bars->kv_full, cb * 64, k0, bkv, once);
-          tma_load_3d(smem + kOffV + cb * kBlock, &tmap_v, &bars->kv_full, cb * 64, k0, bkv, once);
+        mbar_arrive_expect_tx(&bars->kv_full, 2 * C::kTileBytes);
+        for (int cb = 0; cb < D / 64; ++cb) {
+          tma_load_3d(smem + C::kOffK + cb * kBlock, &tmap_k, &bars->kv_full, cb * 64, k0, bkv, once);
+          tma_load_3d(smem + C::kOffV + cb * kBlock, &tmap_v, &bars->kv_full, cb * 64, k0, bkv, once);
         }
       }
       int issued = 0;
       for (int t = 0; t < T; ++t) {
-        const int s = t % kStages;
-        const bool ok = wait_bar(&bars->qd_empty[s], ((t / kStages) & 1) ^ 1, abort_flag, p.status);
+        const int s = t % C::kStages;
+        const bool ok = wait_bar(&bars->qd_empty[s], ((t / C::kStages) & 1) ^ 1, abort_flag, p.status);
         if (!__all_sync(0xffffffffu, ok)) break;
         int h, q0;
         block_coords(t, h, q0);
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * kTileBytes);
-          for (int cb = 0; cb < 2; ++cb) {
-            tma_load_3d(smem + kOffQ + s * kTileBytes + cb * kBlock, &tmap_q, &bars->qd_full[s], cb * 64,
+          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * C::kTileBytes);
+          for (int cb = 0; cb < D / 64; ++cb) {
+            tma_load_3d(smem + C::kOffQ + s * C::kTileBytes + cb * kBlock, &tmap_q, &bars->qd_full[s], cb * 64,
                         q0, b * p.H + h, reuse);
-            tma_load_3d(smem + kOffDO + s * kTileBytes + cb * kBlock, &tmap_do, &bars->qd_full[s],
+            tma_load_3d(smem + C::kOffDO + s * C::kTileBytes + cb * kBlock, &tmap_do, &bars->qd_full[s],
                         cb * 64, q0, b * p.H + h, reuse);
           }
         }
@@ -273,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int dummy = 0;
         volatile int* no_abort = reinterpret_cast<volatile int*>(&dummy);
         bounded_wait(&bars->kv_full, 0, no_abort, p.status, kStatusTimeoutDrain);
-        for (int t = max(0, issued - kStages); t < issued; ++t)
-          bounded_wait(&bars->qd_full[t % kStages], (t / kStages) & 1, no_abort, p.status,
+        for (int t = max(0, issued - C::kStages); t < issued; ++t)
+          bounded_wait(&bars->qd_full[t % C::kStages], (t / C::kStages) & 1, no_abort, p.status,
                        kStatusTimeoutDrain);
       }
       __syncwarp();
@@ -282,14 +285,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ============================================================== MMA issuer
       if (lane == 0 && T > 0) {
         constexpr uint32_t kIdSS = idesc_f16(BF16, false, false, 128, 128);  // S^T, dP^T
-        constexpr uint32_t kIdTS = idesc_f16(BF16, false, true, 128, 128);   // dV, dK
-        const uint64_t dK_A = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
-        const uint64_t dV_A = smem_desc_sw128(smem_u32(smem + kOffV), 16, 1024);
-        const uint32_t aQ0 = smem_u32(smem + kOffQ), aDO0 = smem_u32(smem + kOffDO);
+        constexpr uint32_t kIdTS = idesc_f16(BF16, false, true, 128, D);     // dV, dK
+        const uint64_t dK_A = smem_desc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+        const uint64_t dV_A = smem_desc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
+        const uint32_t aQ0 = smem_u32(smem + C::kOffQ), aDO0 = smem_u32(smem + C::kOffDO);
         auto issue_ss = [&](uint32_t d_col, uint64_t a_desc, uint32_t b_base) {
           const uint64_t bd = smem_desc_sw128(b_base, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
+          for (int kk = 0; kk < D / 16; ++kk)
             mma_f16_ss(tmem + d_col, a_desc + kstep_kmajor(kk), bd + kstep_kmajor(kk), kIdSS, kk > 0 ? 1u : 0u);
         };
         // A from tensor memory: 16 query rows (K) = 8 packed columns; rows
@@ -305,37 +308,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                   wait_bar(&bars->qd_full[0], 0, abort_flag, p.status);
         if (ok) {
           tc_fence_after();
-          issue_ss(kColX, dK_A, aQ0);
+          issue_ss(C::kColX, dK_A, aQ0);
           mma_commit(&bars->s_full);
-          issue_ss(kColY, dV_A, aDO0);
+          issue_ss(C::kColY, dV_A, aDO0);
           mma_commit(&bars->dp_full);
         }
         for (int t = 0; ok && t < T; ++t) {
-          const int s = t % kStages;
+          const int s = t % C::kStages;
           const uint32_t ph = t & 1;
           // dV += P^T dO_t
           if (!(ok = wait_bar(&bars->p_full, ph, abort_flag, p.status))) break;
           tc_fence_after();
-          issue_ts(kColDV, kColX, aDO0 + s * kTileBytes, t > 0);
+          issue_ts(C::kColDV, C::kColX, aDO0 + s * C::kTileBytes, t > 0);
           mma_commit(&bars->dv_done);
           // dK += dS^T Q_t (the last reader of this Q/dO stage)
           if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
           tc_fence_after();
-          issue_ts(kColDK, kColY, aQ0 + s * kTileBytes, t > 0);
+          issue_ts(C::kColDK, C::kColY, aQ0 + s * C::kTileBytes, t > 0);
           mma_commit(&bars->dk_done);
           mma_commit(&bars->qd_empty[s]);
           if (t + 1 < T) {
-            const int s1 = (t + 1) % kStages;
-            if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / kStages) & 1, abort_flag, p.status))) break;
+            const int s1 = (t + 1) % C::kStages;
+            if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / C::kStages) & 1, abort_flag, p.status))) break;
             // S^T(t+1) over P^T(t) once dV has read it; dP^T(t+1) over dS^T(t)
             // once dK has read it
             if (!(ok = wait_bar(&bars->dv_done, ph, abort_flag, p.status))) break;
             tc_fence_after();
-            issue_ss(kColX, dK_A, aQ0 + s1 * kTileBytes);
+            issue_ss(C::kColX, dK_A, aQ0 + s1 * C::kTileBytes);
             mma_commit(&bars->s_full);
             if (!(ok = wait_bar(&bars->dk_done, ph, abort_flag, p.status))) break;
             tc_fence_after();
-            issue_ss(kColY, dV_A, aDO0 + s1 * kTileBytes);
+            issue_ss(C::kColY, dV_A, aDO0 + s1 * C::kTileBytes);
             mma_commit(&bars->dp_full);
           }
         }
@@ -354,19 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kl = (warp % 4) * 32 + lane;  // key row within the tile (= TMEM lane)
     const int key = k0 + kl;
     const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t colX = tmem + lane_off + kColX + wg * 64;
-    const uint32_t colY = tmem + lane_off + kColY + wg * 64;
+    const uint32_t colX = tmem + lane_off + C::kColX + wg * 64;
+    const uint32_t colY = tmem + lane_off + C::kColY + wg * 64;
     const float lam = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
-      const int s = t % kStages;
+      const int s = t % C::kStages;
       const uint32_t ph = t & 1;
       int h, q0;
       block_coords(t, h, q0);
       (void)h;
       const int c0 = q0 + wg * 64;  // query row of this warpgroup's first column
       ok = wait_bar(&bars->s_full, ph, abort_flag, p.status) &&
-           wait_bar(&bars->qd_full[s], (t / kStages) & 1, abort_flag, p.status);
+           wait_bar(&bars->qd_full[s], (t / C::kStages) & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -447,12 +450,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const float mul = wg ? p.scale : 1.f;
     uint16_t* dst = reinterpret_cast<uint16_t*>(wg ? p.dk : p.dv) +
-                    (static_cast<long long>(bkv) * p.Sk + key) * kD;
+                    (static_cast<long long>(bkv) * p.Sk + key) * D;
 #pragma unroll 1
-    for (int c = 0; c < kD / 32; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t w[32];
       if (have) {
-        tmem_ld32(tmem + lane_off + (wg ? kColDK : kColDV) + c * 32, w);
+        tmem_ld32(tmem + lane_off + (wg ? C::kColDK : C::kColDV) + c * 32, w);
         tmem_wait_ld();
         reg_fence32(w);
       } else {
@@ -481,39 +484,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 // =========================================================================
 // Row owner: dQ.
 // =========================================================================
-namespace row {
-constexpr int kStages = 3;                 // K/V stages
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kOffKV = 0;                  // stage s: K at s*64 KiB, V 32 KiB after it
-constexpr int kOffDS = kOffKV + kStages * kStageBytes;  // dS, K-major A of the dQ product
-constexpr int kOffBars = kOffDS + kTileBytes;
-constexpr int kSmemBytes = 1024 + kOffBars + 256;
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-constexpr uint32_t kColDQ = 0, kColS = 128, kColP = 256, kColQ = 384, kColDO = 448;
+template <int D>
+struct RowCfg {
+  static constexpr int kTileBytes = kT * D * 2;        // a 128-key tile of K or V
+  static constexpr int kStages = (D == 128) ? 3 : 5;   // K/V stages
+  static constexpr int kStageBytes = 2 * kTileBytes;   // stage s: K, then V
+  static constexpr int kOffKV = 0;
+  static constexpr int kOffDS = kOffKV + kStages * kStageBytes;  // dS, K-major A of the dQ product
+  static constexpr int kOffBars = kOffDS + kDSBytes;
+  static constexpr int kSmemBytes = 1024 + kOffBars + 256;
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  // TMEM: dQ (D columns), S and dP (128 each), Q and dO (D/2 packed columns each)
+  static constexpr uint32_t kColDQ = 0, kColS = D, kColP = D + 128, kColQ = D + 256, kColDO = D + 256 + D / 2;
 
-struct __align__(8) Bars {
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
-  uint64_t qo_ready;
-  uint64_t s_full, s_free;
-  uint64_t dp_full, dp_free;
-  uint64_t ds_full, ds_free;
-  uint64_t acc_done;
-  uint32_t tmem_base;
-  int abort_flag;
+  struct __align__(8) Bars {
+    uint64_t kv_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t qo_ready;
+    uint64_t s_full, s_free;
+    uint64_t dp_full, dp_free;
+    uint64_t ds_full, ds_free;
+    uint64_t acc_done;
+    uint32_t tmem_base;
+    int abort_flag;
+  };
+  static_assert(sizeof(Bars) <= 256, "barrier block");
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
-}  // namespace row
 
-template <bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                   const BwdParams p) {
-  using namespace row;
+  using C = RowCfg<D>;
+  using Bars = typename C::Bars;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBars);
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBars);
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -539,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 1);
     }
@@ -575,75 +582,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t keep = policy_evict_last();  // K/V: re-read by every query block
         int issued = 0;
         for (int j = 0; j < n; ++j) {
-          const int s = j % kStages;
-          if (!wait_bar(&bars->kv_empty[s], ((j / kStages) & 1) ^ 1, abort_flag, p.status)) break;
-          uint8_t* dst = smem + kOffKV + s * kStageBytes;
-          mbar_arrive_expect_tx(&bars->kv_full[s], 2 * kTileBytes);
-          for (int cb = 0; cb < 2; ++cb) {
+          const int s = j % C::kStages;
+          if (!wait_bar(&bars->kv_empty[s], ((j / C::kStages) & 1) ^ 1, abort_flag, p.status)) break;
+          uint8_t* dst = smem + C::kOffKV + s * C::kStageBytes;
+          mbar_arrive_expect_tx(&bars->kv_full[s], 2 * C::kTileBytes);
+          for (int cb = 0; cb < D / 64; ++cb) {
             tma_load_3d(dst + cb * kBlock, &tmap_k, &bars->kv_full[s], cb * 64, j * kT, b * p.Hkv + kvh, keep);
-            tma_load_3d(dst + kTileBytes + cb * kBlock, &tmap_v, &bars->kv_full[s], cb * 64, j * kT,
+            tma_load_3d(dst + C::kTileBytes + cb * kBlock, &tmap_v, &bars->kv_full[s], cb * 64, j * kT,
                         b * p.Hkv + kvh, keep);
           }
           issued = j + 1;
         }
         int dummy = 0;
         volatile int* no_abort = reinterpret_cast<volatile int*>(&dummy);
-        for (int j = max(0, issued - kStages); j < issued; ++j)
-          bounded_wait(&bars->kv_full[j % kStages], (j / kStages) & 1, no_abort, p.status, kStatusTimeoutDrain);
+        for (int j = max(0, issued - C::kStages); j < issued; ++j)
+          bounded_wait(&bars->kv_full[j % C::kStages], (j / C::kStages) & 1, no_abort, p.status, kStatusTimeoutDrain);
       }
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ============================================================== MMA issuer
       if (lane == 0 && n > 0) {
         constexpr uint32_t kIdK = idesc_f16(BF16, false, false, 128, 128);  // S, dP (B K-major)
-        constexpr uint32_t kIdMN = idesc_f16(BF16, false, true, 128, 128);  // dQ (B MN-major)
-        const uint32_t aKV0 = smem_u32(smem + kOffKV);
+        constexpr uint32_t kIdMN = idesc_f16(BF16, false, true, 128, D);    // dQ (B MN-major)
+        const uint32_t aKV0 = smem_u32(smem + C::kOffKV);
         // A from tensor memory: Q / dO rows hold d along 64 packed columns, a
         // K-step of 16 elements = 8 columns.
         auto issue_scores = [&](uint32_t d_col, uint32_t a_col, uint32_t b_base) {
           const uint64_t bd = smem_desc_sw128(b_base, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
+          for (int kk = 0; kk < D / 16; ++kk)
             mma_f16_ts(tmem + d_col, tmem + a_col + kk * 8, bd + kstep_kmajor(kk), kIdK, kk > 0 ? 1u : 0u);
         };
-        const uint64_t dDS_A = smem_desc_sw128(smem_u32(smem + kOffDS), 16, 1024);
+        const uint64_t dDS_A = smem_desc_sw128(smem_u32(smem + C::kOffDS), 16, 1024);
         auto issue_dq = [&](uint32_t b_base, bool accumulate) {
           const uint64_t bd = smem_desc_sw128(b_base, kBlock, 1024);
 #pragma unroll
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_f16_ss(tmem + kColDQ, dDS_A + kstep_kmajor(kk), bd + kstep_mnmajor(kk), kIdMN,
+            mma_f16_ss(tmem + C::kColDQ, dDS_A + kstep_kmajor(kk), bd + kstep_mnmajor(kk), kIdMN,
                        (accumulate || kk > 0) ? 1u : 0u);
         };
         bool ok = wait_bar(&bars->qo_ready, 0, abort_flag, p.status) &&
                   wait_bar(&bars->kv_full[0], 0, abort_flag, p.status);
         if (ok) {
           tc_fence_after();
-          issue_scores(kColS, kColQ, aKV0);
+          issue_scores(C::kColS, C::kColQ, aKV0);
           mma_commit(&bars->s_full);
-          issue_scores(kColP, kColDO, aKV0 + kTileBytes);
+          issue_scores(C::kColP, C::kColDO, aKV0 + C::kTileBytes);
           mma_commit(&bars->dp_full);
         }
         for (int j = 0; ok && j < n; ++j) {
-          const int s = j % kStages;
+          const int s = j % C::kStages;
           const uint32_t ph = j & 1;
           if (j + 1 < n) {
-            const int s1 = (j + 1) % kStages;
-            if (!(ok = wait_bar(&bars->kv_full[s1], ((j + 1) / kStages) & 1, abort_flag, p.status))) break;
+            const int s1 = (j + 1) % C::kStages;
+            if (!(ok = wait_bar(&bars->kv_full[s1], ((j + 1) / C::kStages) & 1, abort_flag, p.status))) break;
             // S(j+1) once both warpgroups hold S(j) in registers
             if (!(ok = wait_bar(&bars->s_free, ph, abort_flag, p.status))) break;
             tc_fence_after();
-            issue_scores(kColS, kColQ, aKV0 + s1 * kStageBytes);
+            issue_scores(C::kColS, C::kColQ, aKV0 + s1 * C::kStageBytes);
             mma_commit(&bars->s_full);
             // dP(j+1) once both warpgroups hold dP(j) in registers
             if (!(ok = wait_bar(&bars->dp_free, ph, abort_flag, p.status))) break;
             tc_fence_after();
-            issue_scores(kColP, kColDO, aKV0 + s1 * kStageBytes + kTileBytes);
+            issue_scores(C::kColP, C::kColDO, aKV0 + s1 * C::kStageBytes + C::kTileBytes);
             mma_commit(&bars->dp_full);
           }
           // dQ += dS(j) K_j
           if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
           tc_fence_after();
-          issue_dq(aKV0 + s * kStageBytes, j > 0);
+          issue_dq(aKV0 + s * C::kStageBytes, j > 0);
           mma_commit(&bars->ds_free);
           mma_commit(&bars->kv_empty[s]);
         }
@@ -666,10 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The row's Q (warpgroup 0) or dO (warpgroup 1) into tensor memory: the
     // 16-bit pairs in memory are already the packed column words.
     {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(wg ? p.dout : p.q) + grow * kD);
-      const uint32_t colA = tmem + lane_off + (wg ? kColDO : kColQ);
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(wg ? p.dout : p.q) + grow * D);
+      const uint32_t colA = tmem + lane_off + (wg ? C::kColDO : C::kColQ);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; half < D / 64; ++half) {  // 32 packed columns = 64 elements each
         uint32_t w[32];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -689,9 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       Dr = p.Dvec[grow];
     }
     const float lam = p.scale_log2;
-    const uint32_t colS = tmem + lane_off + kColS + wg * 64;
-    const uint32_t colP = tmem + lane_off + kColP + wg * 64;
-    uint8_t* ds_row = smem + kOffDS + wg * kBlock + rl * 128;
+    const uint32_t colS = tmem + lane_off + C::kColS + wg * 64;
+    const uint32_t colP = tmem + lane_off + C::kColP + wg * 64;
+    uint8_t* ds_row = smem + C::kOffDS + wg * kBlock + rl * 128;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const uint32_t ph = j & 1;
@@ -763,19 +770,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(&bars->ds_full);
     }
-    // ---- epilogue: dQ row (x tau); warpgroup wg writes columns [64 wg, 64 wg + 64)
+    // ---- epilogue: dQ row (x tau); warpgroup wg writes columns [wg D/2, (wg + 1) D/2)
     bool have = ok && n > 0;
     if (have) {
       have = wait_bar(&bars->acc_done, 0, abort_flag, p.status);
       have = __all_sync(0xffffffffu, have);
       tc_fence_after();
     }
-    uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) + grow * kD + wg * 64;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) + grow * D + wg * (D / 2);
 #pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < D / 64; ++c) {
       uint32_t w[32];
       if (have) {
-        tmem_ld32(tmem + lane_off + kColDQ + wg * 64 + c * 32, w);
+        tmem_ld32(tmem + lane_off + C::kColDQ + wg * (D / 2) + c * 32, w);
         tmem_wait_ld();
         reg_fence32(w);
       } else {
@@ -842,27 +849,27 @@ int head_group_for(long long per_head_bytes, long long heads) {
   return static_cast<int>(hg < heads ? hg : heads);
 }
 
-template <bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL>
 int launch_bwd_t(const BackwardArgs& a) {
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_3d(&tq, a.q, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
-      !make_tmap_3d(&tdo, a.dout, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
-      !make_tmap_3d(&tk, a.k, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
-      !make_tmap_3d(&tv, a.v, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
+  if (!make_tmap_3d(&tq, a.q, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tdo, a.dout, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tk, a.k, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
+      !make_tmap_3d(&tv, a.v, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
     return -1;
   const long long n_rows = static_cast<long long>(a.B) * a.H * a.Sq;
   {
-    const long long blocks = (n_rows * (kD / 8) + 255) / 256;
+    const long long blocks = (n_rows * (D / 8) + 255) / 256;
     if (blocks > 0x7FFFFFFFLL) return -1;
-    bwd_preprocess_kernel<kD, BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
+    bwd_preprocess_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.Dvec, n_rows);
   }
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             col::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_dq_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             row::kSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             ColCfg<D>::kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(bwd_dq_kernel<D, BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             RowCfg<D>::kSmemBytes) != cudaSuccess)
       return -1;
     attr_set = true;
   }
@@ -887,27 +894,31 @@ int launch_bwd_t(const BackwardArgs& a) {
   p.scale_log2 = a.scale * kLog2e;
   p.status = a.status;
   // column owner: a KV head's group re-reads its query heads' Q and dO
-  p.head_group = head_group_for(static_cast<long long>(p.g) * a.Sq * kD * 4,
+  p.head_group = head_group_for(static_cast<long long>(p.g) * a.Sq * D * 4,
                                 static_cast<long long>(a.B) * a.Hkv);
   const long long grid_a = static_cast<long long>(a.B) * a.Hkv * p.n_ktiles;
   if (grid_a > 0x7FFFFFFFLL) return -1;
-  bwd_dkdv_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid_a), kThreads, col::kSmemBytes, a.stream>>>(
+  bwd_dkdv_kernel<D, BF16, CAUSAL><<<static_cast<unsigned>(grid_a), kThreads, ColCfg<D>::kSmemBytes, a.stream>>>(
       tq, tk, tv, tdo, p);
   // row owner: a query head re-reads its KV head's K and V
   BwdParams pr = p;
-  pr.head_group = head_group_for(static_cast<long long>(a.Sk) * kD * 4, static_cast<long long>(a.B) * a.H);
+  pr.head_group = head_group_for(static_cast<long long>(a.Sk) * D * 4, static_cast<long long>(a.B) * a.H);
   const long long grid_b = static_cast<long long>(a.B) * a.H * p.n_qtiles;
   if (grid_b > 0x7FFFFFFFLL) return -1;
-  bwd_dq_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid_b), kThreads, row::kSmemBytes, a.stream>>>(tk, tv, pr);
+  bwd_dq_kernel<D, BF16, CAUSAL><<<static_cast<unsigned>(grid_b), kThreads, RowCfg<D>::kSmemBytes, a.stream>>>(tk, tv, pr);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace
 
 int launch_backward(const BackwardArgs& a) {
-  if (a.d != kD) return -1;
-  if (a.bf16) return a.causal ? launch_bwd_t<true, true>(a) : launch_bwd_t<true, false>(a);
-  return a.causal ? launch_bwd_t<false, true>(a) : launch_bwd_t<false, false>(a);
+  if (a.d == 128) {
+    if (a.bf16) return a.causal ? launch_bwd_t<128, true, true>(a) : launch_bwd_t<128, true, false>(a);
+    return a.causal ? launch_bwd_t<128, false, true>(a) : launch_bwd_t<128, false, false>(a);
+  }
+  if (a.d != 64) return -1;
+  if (a.bf16) return a.causal ? launch_bwd_t<64, true, true>(a) : launch_bwd_t<64, true, false>(a);
+  return a.causal ? launch_bwd_t<64, false, true>(a) : launch_bwd_t<64, false, false>(a);
 }
 
 }  // namespace gbattn

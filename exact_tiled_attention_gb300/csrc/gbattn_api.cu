@@ -202,7 +202,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* stream) {
   if (B < 1 || H < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return GBATTN_EBADSHAPE;
   if (H % Hkv != 0) return GBATTN_EHEADS;
-  if (d != 128) return GBATTN_EHEADDIM;
+  if (d != 64 && d != 128) return GBATTN_EHEADDIM;
   if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
   const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
@@ -318,7 +318,7 @@ const char* gbattn_error_string(int code) {
     case GBATTN_OK: return "ok";
     case GBATTN_EBADSHAPE: return "bad shape (a size is < 1 or too large)";
     case GBATTN_EHEADS: return "query heads are not a multiple of KV heads";
-    case GBATTN_EHEADDIM: return "unsupported head dimension (64 and 128; backward: 128)";
+    case GBATTN_EHEADDIM: return "unsupported head dimension (only 64 and 128)";
     case GBATTN_EDTYPE: return "unsupported dtype (only fp16 and bf16)";
     case GBATTN_EPOINTER: return "null or misaligned pointer";
     case GBATTN_EWORKSPACE: return "workspace too small (or problem beyond a fixed scratch size)";

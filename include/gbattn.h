@@ -52,7 +52,7 @@ extern "C" {
 #define GBATTN_OK 0
 #define GBATTN_EBADSHAPE (-1)       /* B, H, Hkv, Sq, Sk (or Sk_max) < 1, or a size overflows */
 #define GBATTN_EHEADS (-2)          /* H % Hkv != 0 (M4.4 0x06A admissibility) */
-#define GBATTN_EHEADDIM (-3)        /* d not in {64, 128} (attn_bwd: d != 128) */
+#define GBATTN_EHEADDIM (-3)        /* d not in {64, 128} */
 #define GBATTN_EDTYPE (-4)          /* dtype is neither GBATTN_F16 nor GBATTN_BF16 */
 #define GBATTN_EPOINTER (-5)        /* a required pointer is NULL or not 16-byte aligned */
 #define GBATTN_EWORKSPACE (-6)      /* workspace smaller than the matching *_workspace_bytes() */
@@ -168,7 +168,7 @@ size_t attn_bwd_workspace_bytes(int B, int H, int Sq, int d);
  * scores it needs, so every output element has a single writer and a fixed
  * summation order: results are bitwise repeatable (no atomics, 0x06.1F).
  *
- * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM (d must be 128), EDTYPE,
+ * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM, EDTYPE,
  * EPOINTER (every pointer required; lse 4-byte aligned), EWORKSPACE,
  * EUNSUPPORTED, ELAUNCH.
  */

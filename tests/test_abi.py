@@ -154,7 +154,7 @@ def test_bwd_validation(lib):
     assert _bwd(lib, B=0) == -1
     assert _bwd(lib, Sk=0) == -1
     assert _bwd(lib, H=6, Hkv=4) == -2
-    assert _bwd(lib, d=64) == -3
+    assert _bwd(lib, d=96) == -3
     assert _bwd(lib, dtype=2) == -4
     for name in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv", "ws"):
         assert _bwd(lib, **{name: None}) == -5, name

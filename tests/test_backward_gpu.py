@@ -34,6 +34,12 @@ def _dout(shape, dtype, seed):
 
 
 @pytest.mark.parametrize("shape", [
+    # head dim 64: the tiny fp16 workload, ragged tails, causal, GQA
+    (1, 4, 4, 128, 128, "fp16", False, 64),
+    (1, 2, 2, 300, 300, "fp16", True, 64),
+    (2, 4, 2, 257, 257, "bf16", True, 64),
+    (1, 2, 1, 200, 77, "fp16", True, 64),
+    (1, 1, 1, 1, 1, "fp16", False, 64),
     (1, 1, 1, 128, 128, "bf16", False),
     (1, 2, 2, 300, 300, "bf16", True),     # ragged tails, diagonal blocks
     (1, 2, 2, 300, 300, "fp16", False),
@@ -47,8 +53,8 @@ def _dout(shape, dtype, seed):
     (1, 2, 2, 333, 1, "bf16", False),
 ])
 def test_bwd_small_all_elements(shape):
-    B, H, Hkv, Sq, Sk, dt, causal = shape
-    d = 128
+    B, H, Hkv, Sq, Sk, dt, causal = shape[:7]
+    d = shape[7] if len(shape) > 7 else 128
     q, k, v = make_prefill(B, H, Hkv, Sq, Sk, d, DT[dt], 31, device="cuda")
     do = _dout((B, H, Sq, d), DT[dt], 32)
     scale = 1.0 / math.sqrt(d)
@@ -75,6 +81,8 @@ def test_bwd_key_gradient_sums_to_zero_and_constant_values():
 
 
 @pytest.mark.parametrize("name,kv_ids", [
+    ("tiny_fwd_fp16", [0, 3]),
+    ("prefill_fp16_b1_h8_s4096_d64", [0, 7]),
     ("causal_bf16_b4_h16_s8192_d128", [0, 63]),
     ("gqa_causal_bf16_b2_hq32_hkv8_s4096_d128", [1, 14]),
 ])
