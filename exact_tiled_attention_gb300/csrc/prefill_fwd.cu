@@ -34,7 +34,8 @@
 //
 // Per tile X and key tile j (M4.6 0x08-0x09 roles, own protocol):
 //   MMA X:     QK_X(0); then for j: [S_X(j) copied] QK_X(j+1);
-//              [P_X(j) written] PV_X(j) -> commit p_free_X
+//              [P_X(j) written] PV_X(j) keys [0,64) -> commit p_free_lo_X,
+//              keys [64,128) -> commit p_free_X
 //   softmax X: [S_X(j) ready] load S -> signal S free -> row max ->
 //              [PV_X(j-1) done] rescale O if needed, write P_X(j) -> signal
 // K/V slots are loaded in the order the MMAs need them:
@@ -104,7 +105,8 @@ struct __align__(8) Barriers {
   uint64_t s_full[2];
   uint64_t s_free[2];
   uint64_t p_full[2];
-  uint64_t p_free[2];
+  uint64_t p_free_lo[2];  // P.V has read P keys [0,64)
+  uint64_t p_free[2];     // P.V complete
   uint64_t o_full[2];
   uint64_t mma_done[2];
   uint32_t tmem_base;
@@ -180,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_full[x], 1);
       mbar_init(&bars->s_free[x], kBM);
       mbar_init(&bars->p_full[x], kBM);
+      mbar_init(&bars->p_free_lo[x], 1);
       mbar_init(&bars->p_free[x], 1);
       mbar_init(&bars->o_full[x], 1);
       mbar_init(&bars->mma_done[x], 1);
@@ -284,11 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16_ss(s_col, q_desc + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
         };
-        auto issue_pv = [&](int st, bool accumulate) {
+        // P.V over keys [64 half, 64 half + 64): P column block `half`
+        auto issue_pv_half = [&](int st, int half, bool accumulate) {
           const uint64_t vd = smem_desc_sw128(ring_addr + st * C::kTileBytes, C::kBlockBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t poff = ((kk / 4) * C::kBlockBytes + (kk % 4) * 32) >> 4;
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = half * 4 + k4;
+            const uint64_t poff = (half * C::kBlockBytes + k4 * 32) >> 4;
             mma_f16_ss(o_col, p_desc + poff, vd + ((kk * 2048) >> 4), kIdescPV,
                        (accumulate || kk > 0) ? 1u : 0u);
           }
@@ -328,7 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = bounded_wait(&bars->p_full[x], j & 1, abort_flag, p.status, kStatusTimeoutMma)))
               break;
             tc_fence_after();
-            issue_pv(st, j > 0);
+            // released in halves: the softmax may overwrite P keys [0,64)
+            // while the second half of this product still reads [64,128)
+            issue_pv_half(st, 0, j > 0);
+            mma_commit(&bars->p_free_lo[x]);
+            issue_pv_half(st, 1, true);
             mma_commit(&bars->p_free[x]);
             if (j == nt - 1) mma_commit(&bars->o_full[x]);
             mma_commit(&bars->kv_empty[st]);
@@ -422,50 +431,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       l *= gamma;
-      // ---- P_X(j-1) has been consumed (and O_X is stable) once PV_X(j-1) is done
-      if (j > 0) {
-        ok = bounded_wait(&bars->p_free[x], (j - 1) & 1, abort_flag, p.status, kStatusTimeoutSoftmax);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // correction: O_row *= gamma (warp-uniform path; gamma = 1 rows unchanged)
-        if (__any_sync(0xffffffffu, gamma != 1.f)) {
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t w32[32];
-            tmem_ld32(o_tmem + c * 32, w32);
-            tmem_wait_ld();
-            reg_fence32(w32);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) w32[i] = __float_as_uint(__uint_as_float(w32[i]) * gamma);
-            tmem_st32(o_tmem + c * 32, w32);
-          }
-          tmem_wait_st();
-        }
-      }
-      // ---- P = 2^(lambda*s - lambda*r), row sum, pack to 16 bits, store the
-      // row of P_X(j) into shared memory (swizzled K-major A operand)
+      // ---- P = 2^(lambda*s - lambda*r), row sum, pack to 16 bits, and store
+      // the row of P_X(j) into shared memory (swizzled K-major A operand), one
+      // 64-key column block at a time: block 0 once PV_X(j-1) has read it,
+      // block 1 once PV_X(j-1) is complete (O_X is then stable, so the
+      // correction happens there too).
       const float rs = (r == -INFINITY) ? 0.f : r * lam;
       const float2 lam2 = make_float2(lam, lam);
       const float2 nrs2 = make_float2(-rs, -rs);
       float2 sum4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int ch = 0; ch < kBN / 8; ++ch) {  // 16-byte chunks of 8 keys
-        uint32_t pk[4];
+      for (int blk = 0; blk < kBN / 64; ++blk) {
+        uint32_t pk[32];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = ch * 8 + 2 * i;
-          const float2 t = ex2_pair(ffma2(make_float2(s[c], s[c + 1]), lam2, nrs2), ch * 4 + i);
-          sum4[i] = fadd2(sum4[i], t);
-          pk[i] = pack2<BF16>(t.x, t.y);
+        for (int c8 = 0; c8 < 8; ++c8) {  // 16-byte chunks of 8 keys
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = blk * 64 + c8 * 8 + 2 * i;
+            const float2 t = ex2_pair(ffma2(make_float2(s[c], s[c + 1]), lam2, nrs2), (blk * 8 + c8) * 4 + i);
+            sum4[i] = fadd2(sum4[i], t);
+            pk[c8 * 4 + i] = pack2<BF16>(t.x, t.y);
+          }
         }
-        const int blk = ch / 8, c8 = ch % 8;
-        *reinterpret_cast<uint4*>(p_row + blk * C::kBlockBytes + ((c8 ^ (row & 7)) << 4)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        if (j > 0) {
+          ok = bounded_wait(blk == 0 ? &bars->p_free_lo[x] : &bars->p_free[x], (j - 1) & 1, abort_flag, p.status,
+                            kStatusTimeoutSoftmax);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          if (blk == kBN / 64 - 1) {
+            tc_fence_after();
+            // correction: O_row *= gamma (warp-uniform path; gamma = 1 rows unchanged)
+            if (__any_sync(0xffffffffu, gamma != 1.f)) {
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t w32[32];
+                tmem_ld32(o_tmem + c * 32, w32);
+                tmem_wait_ld();
+                reg_fence32(w32);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w32[i] = __float_as_uint(__uint_as_float(w32[i]) * gamma);
+                tmem_st32(o_tmem + c * 32, w32);
+              }
+              tmem_wait_st();
+            }
+          }
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          *reinterpret_cast<uint4*>(p_row + blk * C::kBlockBytes + ((c8 ^ (row & 7)) << 4)) =
+              make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
       }
+      if (!ok) break;
       const float2 s01 = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
       l += s01.x + s01.y;
       fence_proxy_async_smem();  // P stores -> visible to the tensor core (async proxy)
