@@ -472,6 +472,56 @@ def bench_backward(args, world, rank, peaks, peak_kind, w=None, steps=None, warm
             "l2": l2_note, "clocks": clocks}
 
 
+def bench_fp8(args, world, rank, peaks, peak_kind, w=None, steps=None, warmup=None):
+    """attn_fwd_fp8 on a 128-dim forward workload with its inputs quantized
+    to E4M3 per (batch, KV head); the call includes the V transpose.  FLOPs as
+    for the 16-bit forward; the peak is the measured bf16 burst x 2 (the
+    nominal dense FP8 : BF16 ratio of 4.5 : 2.25 PFLOP/s)."""
+    from exact_tiled_attention_gb300 import attn_fwd_fp8, attn_fwd_fp8_workspace_bytes, gbattn_device_status
+
+    w = w or PREFILL
+    steps = steps or args.steps
+    warmup = warmup if warmup is not None else args.warmup
+    stream = torch.cuda.current_stream()
+    q, k, v = make_workload(w, device="cuda")
+
+    def quant(x):
+        B, Hx, S, d = x.shape
+        g = Hx // w.Hkv
+        amax = x.float().reshape(B, w.Hkv, -1).abs().amax(dim=2).clamp_min(1e-12)
+        ds = (amax / 448.0).contiguous()
+        codes = (x.float().reshape(B, w.Hkv, g, S, d) / ds[:, :, None, None, None]).reshape(x.shape)
+        return codes.to(torch.float8_e4m3fn).contiguous(), ds
+
+    (q8, dq), (k8, dk), (v8, dv) = quant(q), quant(k), quant(v)
+    del q, k, v
+    o = torch.empty(q8.shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(attn_fwd_fp8_workspace_bytes(w.B, w.Hkv, w.Sk, w.d), dtype=torch.uint8, device="cuda")
+    run = lambda: attn_fwd_fp8(q8, k8, v8, dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse,  # noqa: E731
+                               workspace=ws, stream=stream)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    secs = time_steps(run, steps, warmup, world, stream)
+    clocks = sampler.stop()
+    if gbattn_device_status() != 0:
+        raise RuntimeError("a kernel reported a bounded-wait timeout")
+    secs = max_over_ranks(secs, world)
+    flops = prefill_flops(w)
+    per_call = secs / steps
+    achieved = flops / per_call / 1e12
+    peak = 2.0 * peaks["bf16_tflops"]
+    return {"metric": "attention fwd TFLOP/s (FP8 E4M3 inputs)", "workload": w.name + "_e4m3",
+            "value": round(flops * steps * world / secs / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_call": round(per_call * 1e3, 4), "steps": steps, "warmup": warmup, "dtype": "e4m3",
+            "flops_per_call": flops, "kernels_per_call": 2,
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_kind": f"{peak_kind} bf16 burst x 2 (dense FP8 : BF16 = 2); "
+                                      "V transpose included"},
+            "l2": "inputs 256 MiB per call > 129 MB L2; no flush", "clocks": clocks}
+
+
 # --------------------------------------------------------------------------- CPU oracle
 def cpu_oracle_prefill(target_seconds: float, w=None):
     """Time the fp64 oracle on whole heads of the prefill workload (every
@@ -607,6 +657,8 @@ def main():
     ap.add_argument("--impl", choices=["gbattn", "reference"], default="gbattn")
     ap.add_argument("--workload", default="prefill",
                     choices=["prefill", "decode"] + [n for n, w in WORKLOADS.items() if not w.decode])
+    ap.add_argument("--fp8-only", action="store_true",
+                    help="time only attn_fwd_fp8 on the headline forward workload (profiling runs)")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only attn_bwd on the headline forward workload (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -639,6 +691,20 @@ def main():
     from exact_tiled_attention_gb300 import load_library
 
     load_library()  # fail loudly if the CUDA library is missing
+    if args.fp8_only:
+        w2 = PREFILL if args.workload == "prefill" else WORKLOADS[args.workload]
+        if args.batch > 0:
+            import dataclasses
+
+            w2 = dataclasses.replace(w2, B=args.batch)
+        line = bench_fp8(args, world, rank, peaks, peak_kind, w=w2)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+        return
     if args.backward_only:
         w2 = PREFILL if args.workload == "prefill" else WORKLOADS[args.workload]
         if args.batch > 0:
@@ -660,6 +726,8 @@ def main():
                                           steps=max(3, min(args.steps, 20)), warmup=3)
             line["prefill_other"] = [bench_prefill(args, world, rank, peaks, peak_kind, w=w2,
                                                    with_e2e=False) for w2 in OTHER_PREFILL]
+            line["fp8"] = bench_fp8(args, world, rank, peaks, peak_kind, steps=max(3, min(args.steps, 20)),
+                                    warmup=3)
             bw_steps = max(3, min(args.steps, 20))
             line["backward"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
                                                warmup=3) for w2 in BACKWARD]

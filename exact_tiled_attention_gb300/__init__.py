@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     attn_decode_splitkv_noalloc,
     attn_decode_workspace_bytes,
     attn_fwd,
+    attn_fwd_fp8,
+    attn_fwd_fp8_workspace_bytes,
     error_string,
     gbattn_causal_tile_counts,
     gbattn_device_status,

@@ -29,6 +29,7 @@ ERRORS = {
 EXPORTS = ("attn_fwd", "attn_decode_workspace_bytes", "attn_decode_splitkv",
            "attn_decode_splitkv_noalloc", "attn_decode_noalloc_scratch_bytes",
            "attn_bwd_workspace_bytes", "attn_bwd", "gbattn_exp2_paths",
+           "attn_fwd_fp8_workspace_bytes", "attn_fwd_fp8",
            "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_error_string",
            "gbattn_version")
 
@@ -72,6 +73,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
                                  sz, ci, vp]
         lib.attn_bwd.restype = ci
+        lib.attn_fwd_fp8_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.attn_fwd_fp8_workspace_bytes.restype = sz
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, sz, vp]
+        lib.attn_fwd_fp8.restype = ci
         lib.gbattn_exp2_paths.argtypes = [vp, vp, vp, ctypes.c_longlong, vp]
         lib.gbattn_exp2_paths.restype = ci
         lib.gbattn_causal_tile_counts.argtypes = [ci, ci, ci, ci, ll_p, ll_p, ll_p, ll_p, ll_p]
@@ -221,6 +226,53 @@ def attn_decode_splitkv_noalloc(q, k_cache, v_cache, seqlens, scale: float | Non
         int(n_split), dt, _stream_ptr(stream))
     if rc != GBATTN_OK:
         raise GbattnError(rc, "attn_decode_splitkv_noalloc")
+    return out, lse
+
+
+def attn_fwd_fp8_workspace_bytes(B: int, Hkv: int, Sk: int, d: int) -> int:
+    return int(load_library().attn_fwd_fp8_workspace_bytes(B, Hkv, Sk, d))
+
+
+def attn_fwd_fp8(q, k, v, q_descale=None, k_descale=None, v_descale=None, scale: float | None = None,
+                 causal: bool = False, out=None, lse=None, return_lse: bool = True, workspace=None,
+                 stream=None):
+    """FP8 (E4M3) exact attention forward through the C ABI `attn_fwd_fp8`.
+
+    q [B,H,Sq,128], k/v [B,Hkv,Sk,128] torch.float8_e4m3fn CUDA tensors;
+    descales: optional fp32 CUDA tensors [B, Hkv].  Returns (o bf16, lse)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, 4)
+        if t.dtype != torch.float8_e4m3fn:
+            raise TypeError(f"{n} must be torch.float8_e4m3fn")
+    B, H, Sq, d = q.shape
+    Bk, Hkv, Sk, dk = k.shape
+    if k.shape != v.shape or Bk != B or dk != d:
+        raise ValueError("shape mismatch between q, k, v")
+    descales = []
+    for t, n in ((q_descale, "q_descale"), (k_descale, "k_descale"), (v_descale, "v_descale")):
+        if t is None:
+            descales.append(None)
+            continue
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+                and tuple(t.shape) == (B, Hkv)):
+            raise ValueError(f"{n} must be a contiguous fp32 CUDA tensor [B, Hkv]")
+        descales.append(t.data_ptr())
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    lib = load_library()
+    need = int(lib.attn_fwd_fp8_workspace_bytes(B, Hkv, Sk, d))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    rc = lib.attn_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), *descales, out.data_ptr(),
+                          lse.data_ptr() if lse is not None else None, B, H, Hkv, Sq, Sk, d, float(scale),
+                          int(bool(causal)), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                          _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "attn_fwd_fp8")
     return out, lse
 
 

@@ -105,6 +105,22 @@ __global__ void ex2_paths_kernel(const float* __restrict__ x, float* __restrict_
   reinterpret_cast<float2*>(y_hw)[i] = make_float2(ex2_approx(v.x), ex2_approx(v.y));
 }
 
+bool make_tmap_3d_u8(CUtensorMap* map, const void* base, long long inner, int rows, long long outer,
+                     int box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr || (inner % 16) != 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                                 static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(inner)};
+  const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace gbattn
 
 using namespace gbattn;
@@ -237,6 +253,53 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = status;
   return launch_backward(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
+size_t attn_fwd_fp8_workspace_bytes(int B, int Hkv, int Sk, int d) {
+  if (B < 1 || Hkv < 1 || Sk < 1 || d < 1) return 0;
+  const size_t sk_pad = (static_cast<size_t>(Sk) + 127) / 128 * 128;
+  return static_cast<size_t>(B) * Hkv * d * sk_pad;
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* q_descale, const float* k_descale,
+                 const float* v_descale, void* o, float* lse, int B, int H, int Hkv, int Sq, int Sk, int d,
+                 float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return GBATTN_EBADSHAPE;
+  if (H % Hkv != 0) return GBATTN_EHEADS;
+  if (d != 128) return GBATTN_EHEADDIM;
+  const void* ptrs[] = {q, k, v, o, workspace};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return GBATTN_EPOINTER;
+  const void* opt[] = {q_descale, k_descale, v_descale, lse};
+  for (const void* ptr : opt)
+    if (ptr && (reinterpret_cast<uintptr_t>(ptr) & 3u)) return GBATTN_EPOINTER;
+  if (static_cast<long long>(B) * H > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 65535)
+    return GBATTN_EBADSHAPE;
+  if (workspace_bytes < attn_fwd_fp8_workspace_bytes(B, Hkv, Sk, d)) return GBATTN_EWORKSPACE;
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  PrefillFp8Args a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.q_descale = q_descale;
+  a.k_descale = k_descale;
+  a.v_descale = v_descale;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.vt = workspace;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status;
+  return launch_prefill_fp8(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
 int gbattn_causal_tile_counts(int Sq, int Sk, int Br, int Bc, long long* full, long long* partial,

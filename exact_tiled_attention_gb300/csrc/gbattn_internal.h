@@ -61,11 +61,30 @@ struct BackwardArgs {
   int* status;
 };
 
+// Arguments of one FP8 (E4M3) forward launch.
+struct PrefillFp8Args {
+  const void* q;   // E4M3 [B,H,Sq,d]
+  const void* k;   // E4M3 [B,Hkv,Sk,d]
+  const void* v;   // E4M3 [B,Hkv,Sk,d]
+  const float* q_descale;  // [B,Hkv] or nullptr (1.0)
+  const float* k_descale;
+  const float* v_descale;
+  void* o;         // bf16 [B,H,Sq,d]
+  float* lse;
+  int B, H, Hkv, Sq, Sk, d;
+  float scale;
+  int causal;
+  void* vt;        // workspace: E4M3 [B,Hkv,d,Sk_pad], Sk_pad = Sk rounded up to 128
+  cudaStream_t stream;
+  int* status;
+};
+
 // Each returns a cudaError_t / CUresult folded into 0 (ok) or -1 (launch or
 // tensor-map failure).
 int launch_prefill(const PrefillArgs& a);
 int launch_decode(const DecodeArgs& a);
 int launch_backward(const BackwardArgs& a);
+int launch_prefill_fp8(const PrefillFp8Args& a);
 
 // cuTensorMapEncodeTiled fetched once through the runtime's driver entry
 // point (no link-time dependency on libcuda).
@@ -79,5 +98,11 @@ EncodeTiledFn encode_tiled_fn();
 // (64 x box_rows x 1) box and 128-byte swizzle; rows past `rows` read as 0.
 bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, int d, int rows, long long outer,
                   int box_rows);
+
+// 3-D tensor map over a contiguous [outer, rows, inner] byte tensor with a
+// (128 x box_rows x 1) box and 128-byte swizzle; rows past `rows` and bytes
+// past `inner` read as 0.  inner must be a multiple of 16.
+bool make_tmap_3d_u8(CUtensorMap* map, const void* base, long long inner, int rows, long long outer,
+                     int box_rows);
 
 }  // namespace gbattn

@@ -91,6 +91,48 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int dtype, void *stream);
 
 /*
+ * attn_fwd_fp8_workspace_bytes -- bytes of device workspace attn_fwd_fp8
+ * needs: the 8-bit transposed V, B * Hkv * d * Sk_pad with Sk_pad = Sk
+ * rounded up to a multiple of 128.  Returns 0 for invalid sizes.
+ */
+size_t attn_fwd_fp8_workspace_bytes(int B, int Hkv, int Sk, int d);
+
+/*
+ * attn_fwd_fp8 -- exact attention forward with E4M3 (FP8) inputs.
+ *
+ *   q     [B, H,   Sq, d]  E4M3FN codes, input
+ *   k, v  [B, Hkv, Sk, d]  E4M3FN codes, input
+ *   q_descale, k_descale, v_descale  [B, Hkv] fp32 device arrays or NULL
+ *         (NULL = 1): the real values are code * descale of the (batch, KV
+ *         head); a query head h uses the descale of KV head h / (H / Hkv)
+ *   o     [B, H,   Sq, d]  bf16, output
+ *   lse   [B, H,   Sq]     fp32, output (may be NULL): natural-log sum of
+ *         exp(scale * q.k) over the visible keys, with the dequantized q, k
+ *   scale, causal: as for attn_fwd (d must be 128)
+ *   workspace: caller-owned device scratch of at least
+ *         attn_fwd_fp8_workspace_bytes(B, Hkv, Sk, d) bytes, 16-byte aligned;
+ *         it receives V transposed to [B, Hkv, d, Sk_pad] (the K-major P.V
+ *         operand), contents on entry do not matter
+ *
+ * Definition and passages: the FP8 forward of M4.6 "FlashAttention-3/4
+ * Hardware Pipelines" 0x06 -- scores (scale dQ dK) Q8 K8^T in fp32, row
+ * state in fp32, probabilities u = 2^4 exp(S - r) rounded to E4M3 for the
+ * P V product while the row sum accumulates the fp32 u, O = dV (P8 V8) / l
+ * in bf16 (0x06 "Derive Where Every Scale Must Enter", "Why The Source Raises
+ * Softmax Probabilities"); probability offset 4 and conditional-rescale
+ * threshold 4 (log2 units) keep every u <= 256 < 448 (M4.6 0x09 range
+ * contract, E4M3FN row).  The per-(batch, KV head) descale granularity is
+ * that of the pinned public API described in 0x06.
+ *
+ * Errors: GBATTN_EBADSHAPE (also B*Hkv > 65535), EHEADS, EHEADDIM (d != 128),
+ * EPOINTER, EWORKSPACE, EUNSUPPORTED, ELAUNCH.
+ */
+int attn_fwd_fp8(const void *q, const void *k, const void *v, const float *q_descale,
+                 const float *k_descale, const float *v_descale, void *o, float *lse,
+                 int B, int H, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * attn_decode_workspace_bytes -- bytes of device workspace attn_decode_splitkv
  * needs: one fp32 partial state (m, l, o[d]) per (batch, query head, chunk),
  * i.e. B * Hq * n_split * (d + 2) * 4.  Returns 0 for invalid sizes.
