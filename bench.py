@@ -48,7 +48,11 @@ DECODE = WORKLOADS["decode_splitkv_bf16_b64_hq32_hkv8_sk32768_d128"]
 # The other forward workloads, measured in the default run under "prefill_other"
 # (the tiny one is a parity case only: a few microseconds per launch).
 OTHER_PREFILL = [WORKLOADS["prefill_fp16_b1_h8_s4096_d64"],
-                 WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"]]
+                 WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"],
+                 WORKLOADS["noncausal_bf16_b4_h16_s8192_d128"]]
+# The CTA-pair forward (attn_fwd_pair: non-causal, d = 128), measured in the
+# default run under "cta_pair" on the non-causal workload above.
+PAIR = WORKLOADS["noncausal_bf16_b4_h16_s8192_d128"]
 # Backward workloads (d = 128), measured in the default run under "backward".
 BACKWARD = [WORKLOADS["causal_bf16_b4_h16_s8192_d128"], WORKLOADS["gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"],
             WORKLOADS["prefill_fp16_b1_h8_s4096_d64"]]
@@ -256,15 +260,19 @@ def prefill_footprint(w) -> int:
     return prefill_algorithmic_bytes(w)
 
 
-def bench_prefill(args, world, rank, peaks, peak_kind, w=None, with_e2e=True):
-    from exact_tiled_attention_gb300 import attn_fwd, gbattn_device_status
+def bench_prefill(args, world, rank, peaks, peak_kind, w=None, with_e2e=True, pair=False):
+    from exact_tiled_attention_gb300 import attn_fwd, attn_fwd_pair, gbattn_device_status
 
     w = w or PREFILL
     stream = torch.cuda.current_stream()
     q, k, v = make_workload(w, device="cuda")
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device="cuda")
-    run = lambda: attn_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)  # noqa: E731
+    if pair:
+        assert not w.causal and w.d == 128 and not with_e2e
+        run = lambda: attn_fwd_pair(q, k, v, scale=w.scale, out=o, lse=lse, stream=stream)  # noqa: E731
+    else:
+        run = lambda: attn_fwd(q, k, v, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)  # noqa: E731
     flushed = prefill_footprint(w) < 2 * L2_BYTES
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
@@ -288,10 +296,13 @@ def bench_prefill(args, world, rank, peaks, peak_kind, w=None, with_e2e=True):
     peak = peaks["bf16_tflops"]
     key = f"prefill_fwd_kernel<{w.d},{'bf16' if w.dtype == torch.bfloat16 else 'fp16'},"
     key += ("causal>" if w.causal else "noncausal>") + ("" if w is PREFILL else f"@{w.name}")
+    if pair:
+        key = f"prefill_pair_kernel<{'bf16' if w.dtype == torch.bfloat16 else 'fp16'}>@{w.name}"
     traffic = ncu_traffic(key, PREFILL_SOURCES)
     dtype_name = "bf16" if w.dtype == torch.bfloat16 else "fp16"
     if not with_e2e:
-        return {"workload": w.name, "value": round(tflops_job, 3), "unit": "TFLOP/s",
+        return {"workload": w.name, "impl": "cta_pair" if pair else "one_cta", "value": round(tflops_job, 3),
+                "unit": "TFLOP/s",
                 "ms_per_launch": round(per_launch * 1e3, 5), "steps": args.steps, "dtype": dtype_name,
                 "flops_per_launch": flops,
                 "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
@@ -726,6 +737,8 @@ def main():
                                           steps=max(3, min(args.steps, 20)), warmup=3)
             line["prefill_other"] = [bench_prefill(args, world, rank, peaks, peak_kind, w=w2,
                                                    with_e2e=False) for w2 in OTHER_PREFILL]
+            line["cta_pair"] = bench_prefill(args, world, rank, peaks, peak_kind, w=PAIR, with_e2e=False,
+                                             pair=True)
             line["fp8"] = bench_fp8(args, world, rank, peaks, peak_kind, steps=max(3, min(args.steps, 20)),
                                     warmup=3)
             bw_steps = max(3, min(args.steps, 20))

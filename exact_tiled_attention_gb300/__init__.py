@@ -15,6 +15,7 @@ from .binding import (  # noqa: F401
     attn_decode_splitkv_noalloc,
     attn_decode_workspace_bytes,
     attn_fwd,
+    attn_fwd_pair,
     attn_fwd_fp8,
     attn_fwd_fp8_workspace_bytes,
     error_string,

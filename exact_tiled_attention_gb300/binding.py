@@ -26,7 +26,7 @@ ERRORS = {
     -5: "GBATTN_EPOINTER", -6: "GBATTN_EWORKSPACE", -7: "GBATTN_ELAUNCH",
     -8: "GBATTN_EDEVICE_TIMEOUT", -9: "GBATTN_ESPLIT", -10: "GBATTN_EUNSUPPORTED",
 }
-EXPORTS = ("attn_fwd", "attn_decode_workspace_bytes", "attn_decode_splitkv",
+EXPORTS = ("attn_fwd", "attn_fwd_pair", "attn_decode_workspace_bytes", "attn_decode_splitkv",
            "attn_decode_splitkv_noalloc", "attn_decode_noalloc_scratch_bytes",
            "attn_bwd_workspace_bytes", "attn_bwd", "gbattn_exp2_paths",
            "attn_fwd_fp8_workspace_bytes", "attn_fwd_fp8",
@@ -58,6 +58,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         ll_p = ctypes.POINTER(ctypes.c_longlong)
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, ci, vp]
         lib.attn_fwd.restype = ci
+        lib.attn_fwd_pair.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp]
+        lib.attn_fwd_pair.restype = ci
         lib.attn_decode_workspace_bytes.argtypes = [ci, ci, ci, ci]
         lib.attn_decode_workspace_bytes.restype = sz
         lib.attn_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, cf, ci, vp, sz,
@@ -151,6 +153,34 @@ def attn_fwd(q, k, v, scale: float | None = None, causal: bool = False, out=None
                       int(bool(causal)), dt, _stream_ptr(stream))
     if rc != GBATTN_OK:
         raise GbattnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_pair(q, k, v, scale: float | None = None, out=None, lse=None, return_lse: bool = True, stream=None):
+    """Non-causal d = 128 forward on tcgen05 CTA pairs through the C ABI
+    `attn_fwd_pair`; arguments and results as attn_fwd with causal=False."""
+    _check(q, "q", 4)
+    _check(k, "k", 4)
+    _check(v, "v", 4)
+    B, H, Sq, d = q.shape
+    Bk, Hkv, Sk, dk = k.shape
+    if k.shape != v.shape or Bk != B or dk != d:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    dt = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    rc = lib.attn_fwd_pair(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr() if lse is not None else None, B, H, Hkv, Sq, Sk, d, float(scale), dt,
+                           _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "attn_fwd_pair")
     return out, lse
 
 

@@ -162,6 +162,40 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   return launch_prefill(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
+int attn_fwd_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv, int Sq,
+                  int Sk, int d, float scale, int dtype, void* stream) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return GBATTN_EBADSHAPE;
+  if (H % Hkv != 0) return GBATTN_EHEADS;
+  if (d != 128) return GBATTN_EHEADDIM;
+  if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
+  if (!q || !k || !v || !o || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return GBATTN_EPOINTER;
+  if (static_cast<long long>(B) * H > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
+    return GBATTN_EBADSHAPE;
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.d = d;
+  a.scale = scale;
+  a.causal = 0;
+  a.bf16 = dtype == GBATTN_BF16;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status;
+  return launch_prefill_pair(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
 size_t attn_decode_workspace_bytes(int B, int Hq, int n_split, int d) {
   if (B < 1 || Hq < 1 || n_split < 1 || d < 1) return 0;
   return static_cast<size_t>(B) * Hq * n_split * (static_cast<size_t>(d) + 2) * sizeof(float);

@@ -82,6 +82,9 @@ struct PrefillFp8Args {
 // Each returns a cudaError_t / CUresult folded into 0 (ok) or -1 (launch or
 // tensor-map failure).
 int launch_prefill(const PrefillArgs& a);
+// Non-causal d = 128 forward on a tcgen05 CTA pair (prefill_pair.cu); -1 if
+// the arguments are outside that case or a launch failed.
+int launch_prefill_pair(const PrefillArgs& a);
 int launch_decode(const DecodeArgs& a);
 int launch_backward(const BackwardArgs& a);
 int launch_prefill_fp8(const PrefillFp8Args& a);

@@ -47,6 +47,8 @@ WORKLOADS = {
                                              torch.float16, False, seed=2),
     "causal_bf16_b4_h16_s8192_d128": Workload("causal_bf16_b4_h16_s8192_d128", 4, 16, 16, 8192, 8192,
                                               128, torch.bfloat16, True, seed=3),
+    "noncausal_bf16_b4_h16_s8192_d128": Workload("noncausal_bf16_b4_h16_s8192_d128", 4, 16, 16, 8192,
+                                                 8192, 128, torch.bfloat16, False, seed=6),
     "gqa_causal_bf16_b2_hq32_hkv8_s4096_d128": Workload("gqa_causal_bf16_b2_hq32_hkv8_s4096_d128", 2,
                                                         32, 8, 4096, 4096, 128, torch.bfloat16, True,
                                                         seed=4),

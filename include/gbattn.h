@@ -91,6 +91,25 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              int dtype, void *stream);
 
 /*
+ * attn_fwd_pair -- the non-causal attn_fwd with d = 128, computed by pairs of
+ * CTAs that act as one tcgen05 CTA pair (cta_group::2): each pair owns four
+ * 128-row query tiles of one (batch, head), and each of its two CTAs loads
+ * half of every K/V tile.  Same arguments, layout, ownership and outputs as
+ * attn_fwd with causal = 0 (no causal argument); the result is the same
+ * definition (fp32 arithmetic, P rounded to the input dtype for P.V).
+ *
+ * Passages: as attn_fwd, and M4.6 "FlashAttention-3/4 Hardware Pipelines"
+ * 0x08 (the 2-CTA mode of the non-causal d = 128 forward: an M = 256 product
+ * over the pair, each CTA supplying its own rows of A and half of B).
+ *
+ * Errors: GBATTN_EBADSHAPE, EHEADS, EHEADDIM (d != 128), EDTYPE, EPOINTER,
+ * EUNSUPPORTED, ELAUNCH.
+ */
+int attn_fwd_pair(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int H, int Hkv, int Sq, int Sk, int d, float scale,
+                  int dtype, void *stream);
+
+/*
  * attn_fwd_fp8_workspace_bytes -- bytes of device workspace attn_fwd_fp8
  * needs: the 8-bit transposed V, B * Hkv * d * Sk_pad with Sk_pad = Sk
  * rounded up to a multiple of 128.  Returns 0 for invalid sizes.

@@ -76,6 +76,27 @@ def test_attn_fwd_validation(lib):
     assert _fwd(lib, lse=FAKE + 2) == -5
 
 
+def _fwd_pair(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, H=4, Hkv=2, Sq=8, Sk=8, d=128, scale=0.125,
+             dtype=1, stream=None)
+    a.update(kw)
+    return lib.attn_fwd_pair(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Hkv"], a["Sq"],
+                             a["Sk"], a["d"], a["scale"], a["dtype"], a["stream"])
+
+
+def test_attn_fwd_pair_validation(lib):
+    assert _fwd_pair(lib, B=0) == -1
+    assert _fwd_pair(lib, Sk=0) == -1
+    assert _fwd_pair(lib, H=6, Hkv=4) == -2
+    assert _fwd_pair(lib, d=64) == -3  # the CTA-pair path is d = 128 only
+    assert _fwd_pair(lib, d=96) == -3
+    assert _fwd_pair(lib, dtype=2) == -4
+    assert _fwd_pair(lib, v=None) == -5
+    assert _fwd_pair(lib, k=FAKE + 4) == -5
+    if not torch.cuda.is_available():
+        assert _fwd_pair(lib) == -10
+
+
 def _dec(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, Skm=64, d=128,
              scale=0.1, n=4, ws=FAKE, wsb=1 << 20, dtype=1, stream=None)
