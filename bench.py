@@ -674,6 +674,8 @@ def main():
                     help="time only attn_bwd on the headline forward workload (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
+    ap.add_argument("--cta-pair", action="store_true",
+                    help="with a non-causal d=128 --workload: time attn_fwd_pair (CTA pairs) alone")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch size of both workloads (smaller cases for ncu captures)")
@@ -750,7 +752,10 @@ def main():
             import dataclasses
 
             w2 = dataclasses.replace(w2, B=args.batch)
-        line = bench_prefill(args, world, rank, peaks, peak_kind, w=w2)
+        if args.cta_pair:
+            line = bench_prefill(args, world, rank, peaks, peak_kind, w=w2, with_e2e=False, pair=True)
+        else:
+            line = bench_prefill(args, world, rank, peaks, peak_kind, w=w2)
     else:
         line = bench_decode(args, world, rank, peaks, peak_kind)
         if not args.no_secondary:
