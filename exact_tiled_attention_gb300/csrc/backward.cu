@@ -126,18 +126,29 @@ struct ColCfg {
   static constexpr int kOffV = kOffK + kTileBytes;
   static constexpr int kOffQ = kOffV + kTileBytes;                 // kStages tiles
   static constexpr int kOffDO = kOffQ + kStages * kTileBytes;      // kStages tiles
-  static constexpr int kOffStats = kOffDO + kStages * kTileBytes;  // kStages x (128 lse2 + 128 D) fp32
+  // P^T (128 keys x 128 queries, K-major A of dV) is staged in shared memory
+  // when four Q/dO stages leave room for it (d = 64): S^T(t+1) then follows
+  // as soon as S^T(t) has been copied to registers.  With two stages (d = 128)
+  // the next block's Q/dO load would sit on that path, so P^T overwrites S^T
+  // in tensor memory and S^T(t+1) follows dV(t).
+  static constexpr bool kPTSmem = (D == 64);
+  static constexpr int kOffPT = kOffDO + kStages * kTileBytes;
+  static constexpr int kOffStats = kOffPT + (kPTSmem ? kT * kT * 2 : 0);  // kStages x (128 lse2 + 128 D) fp32
   static constexpr int kOffBars = kOffStats + kStages * 2 * kT * 4;
-  static constexpr int kSmemBytes = 1024 + kOffBars + 256;
+  // Alignment slack for the 1024-byte swizzle atoms only where it fits; without
+  // it the kernel checks that the dynamic shared memory base is aligned.
+  static constexpr int kSlack = (1024 + kOffBars + 256 <= 232448) ? 1024 : 0;
+  static constexpr int kSmemBytes = kSlack + kOffBars + 256;
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  // TMEM: dV, dK (D columns each), S^T/P^T and dP^T/dS^T (128 each)
+  // TMEM: dV, dK (D columns each), S^T (-> P^T when kPTSmem is false) and
+  // dP^T/dS^T (128 each)
   static constexpr uint32_t kColDV = 0, kColDK = D, kColX = 2 * D, kColY = 2 * D + 128;
 
   struct __align__(8) Bars {
     uint64_t kv_full;
     uint64_t qd_full[kStages];
     uint64_t qd_empty[kStages];
-    uint64_t s_full, dp_full;
+    uint64_t s_full, s_free, dp_full;
     uint64_t p_full, ds_full;
     uint64_t dv_done, dk_done;
     uint64_t acc_done;
@@ -154,7 +165,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmap_do, const BwdParams p) {
   using C = ColCfg<D>;
   using Bars = typename C::Bars;
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (C::kSlack == 0 && (smem_u32(smem_raw) & 1023u) != 0) {  // uniform over the CTA
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kStatusSmemAlign);
+    return;
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBars);
@@ -192,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->qd_empty[s], 1);
     }
     mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->s_free, 256);
     mbar_init(&bars->dp_full, 1);
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->ds_full, 256);
@@ -313,33 +329,78 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_ss(C::kColY, dV_A, aDO0);
           mma_commit(&bars->dp_full);
         }
-        for (int t = 0; ok && t < T; ++t) {
-          const int s = t % C::kStages;
-          const uint32_t ph = t & 1;
-          // dV += P^T dO_t
-          if (!(ok = wait_bar(&bars->p_full, ph, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_ts(C::kColDV, C::kColX, aDO0 + s * C::kTileBytes, t > 0);
-          mma_commit(&bars->dv_done);
-          // dK += dS^T Q_t (the last reader of this Q/dO stage)
-          if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
-          tc_fence_after();
-          issue_ts(C::kColDK, C::kColY, aQ0 + s * C::kTileBytes, t > 0);
-          mma_commit(&bars->dk_done);
-          mma_commit(&bars->qd_empty[s]);
-          if (t + 1 < T) {
+        if constexpr (C::kPTSmem) {
+          // dV += P^T dO: A = P^T in shared memory (K-major, two 64-query column
+          // blocks), B = dO (MN-major).
+          const uint64_t pt_desc = smem_desc_sw128(smem_u32(smem + C::kOffPT), 16, 1024);
+          auto issue_dv = [&](uint32_t b_base, bool accumulate) {
+            const uint64_t bd = smem_desc_sw128(b_base, kBlock, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_f16_ss(tmem + C::kColDV, pt_desc + kstep_kmajor(kk), bd + kstep_mnmajor(kk), kIdTS,
+                         (accumulate || kk > 0) ? 1u : 0u);
+          };
+          for (int t = 0; ok && t < T; ++t) {
+            const int s = t % C::kStages;
+            const uint32_t ph = t & 1;
             const int s1 = (t + 1) % C::kStages;
-            if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / C::kStages) & 1, abort_flag, p.status))) break;
-            // S^T(t+1) over P^T(t) once dV has read it; dP^T(t+1) over dS^T(t)
-            // once dK has read it
-            if (!(ok = wait_bar(&bars->dv_done, ph, abort_flag, p.status))) break;
+            // S^T(t+1) as soon as both warpgroups hold S^T(t) in registers (P^T
+            // lives in shared memory, so the S^T columns are free then)
+            if (t + 1 < T) {
+              if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / C::kStages) & 1, abort_flag, p.status))) break;
+              if (!(ok = wait_bar(&bars->s_free, ph, abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_ss(C::kColX, dK_A, aQ0 + s1 * C::kTileBytes);
+              mma_commit(&bars->s_full);
+            }
+            // dV += P^T(t) dO_t
+            if (!(ok = wait_bar(&bars->p_full, ph, abort_flag, p.status))) break;
             tc_fence_after();
-            issue_ss(C::kColX, dK_A, aQ0 + s1 * C::kTileBytes);
-            mma_commit(&bars->s_full);
-            if (!(ok = wait_bar(&bars->dk_done, ph, abort_flag, p.status))) break;
+            issue_dv(aDO0 + s * C::kTileBytes, t > 0);
+            mma_commit(&bars->dv_done);
+            // dK += dS^T Q_t (the last reader of this Q/dO stage)
+            if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
             tc_fence_after();
-            issue_ss(C::kColY, dV_A, aDO0 + s1 * C::kTileBytes);
-            mma_commit(&bars->dp_full);
+            issue_ts(C::kColDK, C::kColY, aQ0 + s * C::kTileBytes, t > 0);
+            mma_commit(&bars->dk_done);
+            mma_commit(&bars->qd_empty[s]);
+            // dP^T(t+1) over dS^T(t) once dK has read it
+            if (t + 1 < T) {
+              if (!(ok = wait_bar(&bars->dk_done, ph, abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_ss(C::kColY, dV_A, aDO0 + s1 * C::kTileBytes);
+              mma_commit(&bars->dp_full);
+            }
+          }
+        } else {
+          for (int t = 0; ok && t < T; ++t) {
+            const int s = t % C::kStages;
+            const uint32_t ph = t & 1;
+            // dV += P^T dO_t
+            if (!(ok = wait_bar(&bars->p_full, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_ts(C::kColDV, C::kColX, aDO0 + s * C::kTileBytes, t > 0);
+            mma_commit(&bars->dv_done);
+            // dK += dS^T Q_t (the last reader of this Q/dO stage)
+            if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            issue_ts(C::kColDK, C::kColY, aQ0 + s * C::kTileBytes, t > 0);
+            mma_commit(&bars->dk_done);
+            mma_commit(&bars->qd_empty[s]);
+            if (t + 1 < T) {
+              const int s1 = (t + 1) % C::kStages;
+              if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / C::kStages) & 1, abort_flag, p.status))) break;
+              // S^T(t+1) over P^T(t) once dV has read it; dP^T(t+1) over dS^T(t)
+              // once dK has read it
+              if (!(ok = wait_bar(&bars->dv_done, ph, abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_ss(C::kColX, dK_A, aQ0 + s1 * C::kTileBytes);
+              mma_commit(&bars->s_full);
+              if (!(ok = wait_bar(&bars->dk_done, ph, abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_ss(C::kColY, dV_A, aDO0 + s1 * C::kTileBytes);
+              mma_commit(&bars->dp_full);
+            }
           }
         }
         mma_commit(&bars->acc_done);
@@ -384,6 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
       reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      if constexpr (C::kPTSmem) {
+        tc_fence_before();
+        mbar_arrive(&bars->s_free);  // S^T(t) copied: the issuer may write S^T(t+1)
+      }
       // P = 2^(lambda s - LSE log2 e); masked: keys past Sk, and (causal)
       // column c with c0 + c + delta < key.
       const bool need_mask = (k0 + kT > p.Sk) || (CAUSAL && (k0 + kT - 1 > c0 + p.delta));
@@ -401,16 +466,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[c + 1] = (need_mask && c + 1 < first_c) ? 0.f : e.y;
         }
       }
-      {
-        uint32_t pk[16];
-        pack32<BF16>(x, 0, pk);
-        tmem_st16(colX, pk);  // P^T over this warpgroup's own S^T columns
-        pack32<BF16>(x, 32, pk);
-        tmem_st16(colX + 16, pk);
+      if constexpr (C::kPTSmem) {
+        {
+          // P^T row of this key, queries [64 wg, 64 wg + 64): 128 bytes of the
+          // warpgroup's column block, 16-byte chunk c at chunk c ^ (key row % 8),
+          // once dV(t-1) has read P^T(t-1)
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack2<BF16>(x[2 * i], x[2 * i + 1]);
+          if (t > 0) {
+            ok = wait_bar(&bars->dv_done, (t - 1) & 1, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+          }
+          uint8_t* pt_row = smem + C::kOffPT + wg * kBlock + kl * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(pt_row + ((c ^ (kl & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_proxy_async_smem();  // P^T stores -> visible to the tensor core
+        mbar_arrive(&bars->p_full);
+      } else {
+        {
+          uint32_t pk[16];
+          pack32<BF16>(x, 0, pk);
+          tmem_st16(colX, pk);  // P^T over this warpgroup's own S^T columns
+          pack32<BF16>(x, 32, pk);
+          tmem_st16(colX + 16, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full);
       // dP^T -> dS^T, 32 columns at a time
       ok = wait_bar(&bars->dp_full, ph, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) {

@@ -21,6 +21,7 @@ enum DeviceStatus : int {
   kStatusTimeoutDrain = 4,    // teardown wait for in-flight copies or MMAs
   kStatusTimeoutDecode = 5,   // decode consumer/producer wait
   kStatusTimeoutBwd = 6,      // backward kernel wait (any role)
+  kStatusSmemAlign = 7,       // dynamic shared memory base not 1024-byte aligned (kernel did nothing)
 };
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.
