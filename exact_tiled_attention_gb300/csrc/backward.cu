@@ -72,6 +72,7 @@ constexpr int kT = 128;      // rows (keys or queries) per tile; head dimension 
 constexpr int kThreads = 384;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kMmaWarpY = 10;  // column owner, d = 128: issuer of the dP^T / dK chain
 constexpr int kRegsCompute = 184, kRegsCtl = 136;
 static_assert(2 * 128 * kRegsCompute + 128 * kRegsCtl <= kThreads * 168, "register split");
 constexpr float kLog2e = 1.4426950408889634f;
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->kv_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->qd_full[s], 1 + 32);  // TMA arrive + 32 lanes' stat stores
-      mbar_init(&bars->qd_empty[s], 1);
+      mbar_init(&bars->qd_empty[s], C::kPTSmem ? 1 : 2);  // d = 128: released by both issuers
     }
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->s_free, 256);
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dv_done, 1);
     mbar_init(&bars->dk_done, 1);
-    mbar_init(&bars->acc_done, 1);
+    mbar_init(&bars->acc_done, C::kPTSmem ? 1 : 2);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -297,8 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                        kStatusTimeoutDrain);
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // ============================================================== MMA issuer
+    } else if (warp == kMmaWarp || (!C::kPTSmem && warp == kMmaWarpY)) {
+      // ============================================================== MMA issuers
+      // d = 64: warp 9 issues everything.  d = 128: warp 9 issues the S^T / dV
+      // chain and warp 10 the dP^T / dK chain, so that neither waits behind
+      // the other's barrier (P^T and dS^T overwrite S^T and dP^T in TMEM).
+      const bool chain_x = warp == kMmaWarp;
       if (lane == 0 && T > 0) {
         constexpr uint32_t kIdSS = idesc_f16(BF16, false, false, 128, 128);  // S^T, dP^T
         constexpr uint32_t kIdTS = idesc_f16(BF16, false, true, 128, D);     // dV, dK
@@ -324,10 +329,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                   wait_bar(&bars->qd_full[0], 0, abort_flag, p.status);
         if (ok) {
           tc_fence_after();
-          issue_ss(C::kColX, dK_A, aQ0);
-          mma_commit(&bars->s_full);
-          issue_ss(C::kColY, dV_A, aDO0);
-          mma_commit(&bars->dp_full);
+          if (chain_x) {
+            issue_ss(C::kColX, dK_A, aQ0);
+            mma_commit(&bars->s_full);
+          }
+          if (C::kPTSmem || !chain_x) {
+            issue_ss(C::kColY, dV_A, aDO0);
+            mma_commit(&bars->dp_full);
+          }
         }
         if constexpr (C::kPTSmem) {
           // dV += P^T dO: A = P^T in shared memory (K-major, two 64-query column
@@ -372,30 +381,40 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_commit(&bars->dp_full);
             }
           }
-        } else {
+        } else if (chain_x) {
           for (int t = 0; ok && t < T; ++t) {
             const int s = t % C::kStages;
             const uint32_t ph = t & 1;
-            // dV += P^T dO_t
+            // dV += P^T dO_t (this chain's last reader of the stage)
             if (!(ok = wait_bar(&bars->p_full, ph, abort_flag, p.status))) break;
             tc_fence_after();
             issue_ts(C::kColDV, C::kColX, aDO0 + s * C::kTileBytes, t > 0);
             mma_commit(&bars->dv_done);
-            // dK += dS^T Q_t (the last reader of this Q/dO stage)
+            mma_commit(&bars->qd_empty[s]);
+            // S^T(t+1) over P^T(t) once dV has read it
+            if (t + 1 < T) {
+              const int s1 = (t + 1) % C::kStages;
+              if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / C::kStages) & 1, abort_flag, p.status))) break;
+              if (!(ok = wait_bar(&bars->dv_done, ph, abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_ss(C::kColX, dK_A, aQ0 + s1 * C::kTileBytes);
+              mma_commit(&bars->s_full);
+            }
+          }
+        } else {
+          for (int t = 0; ok && t < T; ++t) {
+            const int s = t % C::kStages;
+            const uint32_t ph = t & 1;
+            // dK += dS^T Q_t (this chain's last reader of the stage)
             if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
             tc_fence_after();
             issue_ts(C::kColDK, C::kColY, aQ0 + s * C::kTileBytes, t > 0);
             mma_commit(&bars->dk_done);
             mma_commit(&bars->qd_empty[s]);
+            // dP^T(t+1) over dS^T(t) once dK has read it
             if (t + 1 < T) {
               const int s1 = (t + 1) % C::kStages;
               if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / C::kStages) & 1, abort_flag, p.status))) break;
-              // S^T(t+1) over P^T(t) once dV has read it; dP^T(t+1) over dS^T(t)
-              // once dK has read it
-              if (!(ok = wait_bar(&bars->dv_done, ph, abort_flag, p.status))) break;
-              tc_fence_after();
-              issue_ss(C::kColX, dK_A, aQ0 + s1 * C::kTileBytes);
-              mma_commit(&bars->s_full);
               if (!(ok = wait_bar(&bars->dk_done, ph, abort_flag, p.status))) break;
               tc_fence_after();
               issue_ss(C::kColY, dV_A, aDO0 + s1 * C::kTileBytes);
