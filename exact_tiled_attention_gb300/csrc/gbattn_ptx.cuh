@@ -111,6 +111,17 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// 3-D tiled store of one box from shared memory (same box and swizzle as the
+// map's loads); elements outside the tensor are not written.  x must be a
+// multiple of 16 bytes and no coordinate may be negative.  Tracked by the
+// issuing thread's bulk async-group (commit / wait below).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // L2 eviction-priority policies (createpolicy).
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;

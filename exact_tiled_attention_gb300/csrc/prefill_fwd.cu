@@ -137,7 +137,8 @@ template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmap_q,
                        const __grid_constant__ CUtensorMap tmap_k,
-                       const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+                       const __grid_constant__ CUtensorMap tmap_v,
+                       const __grid_constant__ CUtensorMap tmap_o, const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -194,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tmap_q);
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
+    prefetch_tensormap(&tmap_o);
   }
   if (warp == kMmaWarpH) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -502,27 +504,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool row_ok = q_row < p.Sq;
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      using T = uint16_t;
-      T* orow = reinterpret_cast<T*>(p.o) + ((static_cast<size_t>(b) * p.H + h) * p.Sq + (row_ok ? q_row : 0)) * D;
+      // d = 64 (measured faster): O_X is staged in Q_X (dead since QK_X of the
+      // last key tile completed) and written by TMA; d = 128 (measured faster
+      // this way): each thread stores its row directly.
+      if constexpr (D == 64) {
+        // O_X is staged in Q_X (dead since QK_X of the last key tile completed)
+        // in the Q layout -- 64-element column blocks of 128-byte rows, 16-byte
+        // chunk c at chunk c ^ (row % 8) -- and written by one TMA store per
+        // column block (rows past Sq are not written).
+        uint8_t* o_row = sQ + x * C::kTileBytes + row * 128;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        if (have_o) {
-          tmem_ld32(o_tmem + c * 32, u);
-          tmem_wait_ld();
-          reg_fence32(u);
-        } else {
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          if (have_o) {
+            tmem_ld32(o_tmem + c * 32, u);
+            tmem_wait_ld();
+            reg_fence32(u);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) u[i] = 0u;
+            for (int i = 0; i < 32; ++i) u[i] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+          uint8_t* blk = o_row + (c / 2) * C::kBlockBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int ch = (c % 2) * 4 + k;
+            *reinterpret_cast<uint4*>(blk + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          }
         }
-        uint32_t pk[16];
+        fence_proxy_async_smem();    // O stores -> visible to the TMA engine
+        named_bar_sync(1 + x, kBM);  // the four warps of the tile have written O_X
+        if (wq == 0 && lane == 0) {
+          for (int cb = 0; cb < C::kColBlocks; ++cb)
+            tma_store_3d(&tmap_o, sQ + x * C::kTileBytes + cb * C::kBlockBytes, cb * 64, q0x, b * p.H + h);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // shared memory read before the CTA may exit
+        }
+      } else {
+        using T = uint16_t;
+        T* orow = reinterpret_cast<T*>(p.o) + ((static_cast<size_t>(b) * p.H + h) * p.Sq + (row_ok ? q_row : 0)) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          if (have_o) {
+            tmem_ld32(o_tmem + c * 32, u);
+            tmem_wait_ld();
+            reg_fence32(u);
+          } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+            for (int i = 0; i < 32; ++i) u[i] = 0u;
+          }
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
         }
       }
       if (row_ok && p.lse != nullptr) {
@@ -542,8 +586,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool BF16, bool CAUSAL>
 int launch_t(const PrefillArgs& a) {
   using C = Cfg<D>;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_tmap_3d(&tq, a.q, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
+      !make_tmap_3d(&to, a.o, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
       !make_tmap_3d(&tk, a.k, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN) ||
       !make_tmap_3d(&tv, a.v, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN))
     return -1;
@@ -580,7 +625,7 @@ int launch_t(const PrefillArgs& a) {
   p.status = a.status;
   const long long grid = static_cast<long long>(a.B) * a.H * p.n_pairs;
   if (grid > 0x7FFFFFFFLL) return -1;
-  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, p);
+  kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
