@@ -172,13 +172,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nt_l = tiles_for(q0_l, p.Sq, p.Sk, CAUSAL ? 1 : 0, p.delta);
   const int n_max = max(nt_h, nt_l);
 
-  // ---- setup
-  if (threadIdx.x == 0) {
+  // ---- K/V load items in the order K_0, K_1, V_0, K_2, V_1, ... (loader lane)
+  const int n_items = 2 * n_max;
+  auto issue_item = [&](int it, uint64_t policy) {
+    const int st = it % C::kStages;
+    bool is_v;
+    int jt;
+    if (it == 0) {
+      is_v = false, jt = 0;
+    } else if (it & 1) {
+      if (it == n_items - 1) is_v = true, jt = n_max - 1;
+      else is_v = false, jt = (it + 1) / 2;
+    } else {
+      is_v = true, jt = (it - 2) / 2;
+    }
+    mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
+    for (int cb = 0; cb < C::kColBlocks; ++cb)
+      tma_load_3d(sRing + st * C::kTileBytes + cb * C::kBlockBytes, is_v ? &tmap_v : &tmap_k, &bars->kv_full[st],
+                  cb * 64, jt * kBN, b * p.Hkv + kvh, policy);
+  };
+
+  // ---- setup.  The loader lane initialises the load barriers itself and
+  // requests Q and the first ring's worth of K/V (whose slots start free)
+  // before the CTA-wide barrier, so those copies overlap the TMEM allocation
+  // and the barrier.
+  int pre_issued = 0;
+  if (warp == kLoadWarp && lane == 0) {
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->kv_full[s], 1);
       mbar_init(&bars->kv_empty[s], 2);  // released by both MMA issuers
     }
+    fence_mbar_init();
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+    prefetch_tensormap(&tmap_o);
+    const uint64_t once = policy_evict_first();  // Q: read by this CTA only
+    uint32_t q_bytes = 0;
+    q_bytes += nt_h > 0 ? C::kTileBytes : 0;
+    q_bytes += nt_l > 0 ? C::kTileBytes : 0;
+    mbar_arrive_expect_tx(&bars->q_full, q_bytes);
+    for (int x = 0; x < 2; ++x) {
+      if ((x ? nt_l : nt_h) == 0) continue;
+      for (int cb = 0; cb < C::kColBlocks; ++cb)
+        tma_load_3d(sQ + x * C::kTileBytes + cb * C::kBlockBytes, &tmap_q, &bars->q_full, cb * 64,
+                    x ? q0_l : q0_h, b * p.H + h, once);
+    }
+    const uint64_t keep = policy_evict_last();  // K/V: re-read by other CTAs
+    pre_issued = min(C::kStages, n_items);
+    for (int it = 0; it < pre_issued; ++it) issue_item(it, keep);
+  }
+  if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
       mbar_init(&bars->s_full[x], 1);
       mbar_init(&bars->s_free[x], kBM);
@@ -190,12 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     bars->abort_flag = 0;
     fence_mbar_init();
-  }
-  if (warp == kLoadWarp && lane == 0) {
-    prefetch_tensormap(&tmap_q);
-    prefetch_tensormap(&tmap_k);
-    prefetch_tensormap(&tmap_v);
-    prefetch_tensormap(&tmap_o);
   }
   if (warp == kMmaWarpH) {
     tmem_alloc(&bars->tmem_base, 512);
@@ -212,40 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kLoadWarp) {
       // ================================================================ loader
       if (lane == 0) {
-        const uint64_t keep = policy_evict_last();   // K/V: re-read by other CTAs
-        const uint64_t once = policy_evict_first();  // Q: read by this CTA only
-        uint32_t q_bytes = 0;
-        q_bytes += nt_h > 0 ? C::kTileBytes : 0;
-        q_bytes += nt_l > 0 ? C::kTileBytes : 0;
-        mbar_arrive_expect_tx(&bars->q_full, q_bytes);
-        for (int x = 0; x < 2; ++x) {
-          if ((x ? nt_l : nt_h) == 0) continue;
-          for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(sQ + x * C::kTileBytes + cb * C::kBlockBytes, &tmap_q, &bars->q_full, cb * 64,
-                        x ? q0_l : q0_h, b * p.H + h, once);
-        }
-        const int n_items = 2 * n_max;
-        int issued = 0;
-        for (int it = 0; it < n_items; ++it) {
+        const uint64_t keep = policy_evict_last();  // K/V: re-read by other CTAs
+        int issued = pre_issued;
+        for (int it = pre_issued; it < n_items; ++it) {
           const int st = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
           if (!bounded_wait(&bars->kv_empty[st], ph ^ 1, abort_flag, p.status, kStatusTimeoutLoad))
             break;
-          // item -> (K or V, key tile) in the order K_0, K_1, V_0, K_2, V_1, ...
-          bool is_v;
-          int jt;
-          if (it == 0) {
-            is_v = false, jt = 0;
-          } else if (it & 1) {
-            if (it == n_items - 1) is_v = true, jt = n_max - 1;
-            else is_v = false, jt = (it + 1) / 2;
-          } else {
-            is_v = true, jt = (it - 2) / 2;
-          }
-          mbar_arrive_expect_tx(&bars->kv_full[st], C::kTileBytes);
-          for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_load_3d(sRing + st * C::kTileBytes + cb * C::kBlockBytes, is_v ? &tmap_v : &tmap_k,
-                        &bars->kv_full[st], cb * 64, jt * kBN, b * p.Hkv + kvh, keep);
+          issue_item(it, keep);
           issued = it + 1;
         }
         // Drain: every copy this thread issued must have landed before exit.
