@@ -35,8 +35,10 @@
  *    gets O = 0 and LSE = -inf.
  *  - Return value: GBATTN_OK or a negative GBATTN_E* code.  Argument errors
  *    are detected on the host before anything is enqueued.  Asynchronous
- *    device-side failures (a bounded wait inside a kernel that timed out) are
- *    reported by gbattn_device_status() after the caller synchronises.
+ *    device-side failures (a bounded wait inside a kernel that timed out, or
+ *    a dynamic shared-memory base without the 1024-byte alignment a kernel
+ *    relies on, in which case that kernel writes nothing) are reported by
+ *    gbattn_device_status() after the caller synchronises.
  */
 #ifndef GBATTN_H_
 #define GBATTN_H_
@@ -57,7 +59,8 @@ extern "C" {
 #define GBATTN_EPOINTER (-5)        /* a required pointer is NULL or not 16-byte aligned */
 #define GBATTN_EWORKSPACE (-6)      /* workspace smaller than the matching *_workspace_bytes() */
 #define GBATTN_ELAUNCH (-7)         /* the CUDA runtime rejected a launch or a tensor map */
-#define GBATTN_EDEVICE_TIMEOUT (-8) /* a kernel's bounded wait gave up (gbattn_device_status) */
+#define GBATTN_EDEVICE_TIMEOUT (-8) /* a kernel gave up on device: a bounded wait timed out, or its
+                                       shared-memory base was not 1024-byte aligned (gbattn_device_status) */
 #define GBATTN_ESPLIT (-9)          /* decode n_split < 1 or > 256 */
 #define GBATTN_EUNSUPPORTED (-10)   /* no sm_103a device, or the current device is not sm_103 */
 
@@ -300,8 +303,9 @@ int gbattn_exp2_paths(const float *x, float *y_poly, float *y_hw, long long n, v
 /*
  * gbattn_device_status -- read and clear the library's device status word
  * (synchronises the current device).  Returns GBATTN_OK, or
- * GBATTN_EDEVICE_TIMEOUT if a kernel gave up a bounded wait since the last
- * call, or GBATTN_ELAUNCH if the device reported an error.
+ * GBATTN_EDEVICE_TIMEOUT if a kernel gave up since the last call (a bounded
+ * wait timed out, or a shared-memory alignment check failed), or
+ * GBATTN_ELAUNCH if the device reported an error.
  */
 int gbattn_device_status(void);
 
