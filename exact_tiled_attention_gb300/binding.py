@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libgbattn.so")
 GBATTN_OK = 0
 GBATTN_F16 = 0
 GBATTN_BF16 = 1
+GBATTN_EDEVICE_TIMEOUT = -8
 ERRORS = {
     -1: "GBATTN_EBADSHAPE", -2: "GBATTN_EHEADS", -3: "GBATTN_EHEADDIM", -4: "GBATTN_EDTYPE",
     -5: "GBATTN_EPOINTER", -6: "GBATTN_EWORKSPACE", -7: "GBATTN_ELAUNCH",
@@ -29,7 +30,7 @@ ERRORS = {
 EXPORTS = ("attn_fwd", "attn_fwd_pair", "attn_decode_workspace_bytes", "attn_decode_splitkv",
            "attn_decode_splitkv_noalloc", "attn_decode_noalloc_scratch_bytes",
            "attn_bwd_workspace_bytes", "attn_bwd", "gbattn_exp2_paths",
-           "attn_fwd_fp8_workspace_bytes", "attn_fwd_fp8",
+           "attn_fwd_fp8_workspace_bytes", "attn_fwd_fp8", "gbattn_selftest_bounded_wait",
            "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_error_string",
            "gbattn_version")
 
@@ -83,6 +84,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gbattn_exp2_paths.restype = ci
         lib.gbattn_causal_tile_counts.argtypes = [ci, ci, ci, ci, ll_p, ll_p, ll_p, ll_p, ll_p]
         lib.gbattn_causal_tile_counts.restype = ci
+        lib.gbattn_selftest_bounded_wait.argtypes = [ci, vp]
+        lib.gbattn_selftest_bounded_wait.restype = ci
         lib.gbattn_device_status.argtypes = []
         lib.gbattn_device_status.restype = ci
         lib.gbattn_error_string.argtypes = [ci]
@@ -370,6 +373,14 @@ def gbattn_exp2_paths(x, stream=None):
     if rc != GBATTN_OK:
         raise GbattnError(rc, "gbattn_exp2_paths")
     return y_poly, y_hw
+
+
+def gbattn_selftest_bounded_wait(arrive: bool, stream=None) -> None:
+    """Diagnostic: one bounded mbarrier wait on the device that nothing
+    satisfies unless `arrive`; read the outcome with gbattn_device_status()."""
+    rc = load_library().gbattn_selftest_bounded_wait(int(bool(arrive)), _stream_ptr(stream))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "gbattn_selftest_bounded_wait")
 
 
 def gbattn_device_status() -> int:

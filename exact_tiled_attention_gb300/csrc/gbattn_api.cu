@@ -389,6 +389,31 @@ int gbattn_exp2_paths(const float* x, float* y_poly, float* y_hw, long long n, v
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
+// One warp: thread 0 waits (bounded) on an mbarrier that completes only if
+// `arrive` is set -- the wait every kernel role performs on its producer.
+__global__ void selftest_wait_kernel(int arrive, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (arrive) mbar_arrive(&bar);
+    bounded_wait(&bar, 0, &abort_flag, status, kStatusSelftest);
+  }
+}
+
+int gbattn_selftest_bounded_wait(int arrive, void* stream) {
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(arrive ? 1 : 0, status);
+  return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
 int gbattn_device_status(void) {
   int* status = nullptr;
   int rc = current_device(&status);
@@ -420,7 +445,7 @@ const char* gbattn_error_string(int code) {
     case GBATTN_EPOINTER: return "null or misaligned pointer";
     case GBATTN_EWORKSPACE: return "workspace too small (or problem beyond a fixed scratch size)";
     case GBATTN_ELAUNCH: return "CUDA launch or tensor-map encoding failed";
-    case GBATTN_EDEVICE_TIMEOUT: return "a kernel's bounded wait timed out";
+    case GBATTN_EDEVICE_TIMEOUT: return "a kernel gave up on the device (bounded wait timed out or shared memory misaligned)";
     case GBATTN_ESPLIT: return "n_split out of range (1..256)";
     case GBATTN_EUNSUPPORTED: return "no sm_103 device is current";
     default: return "unknown status code";

@@ -22,6 +22,7 @@ enum DeviceStatus : int {
   kStatusTimeoutDecode = 5,   // decode consumer/producer wait
   kStatusTimeoutBwd = 6,      // backward kernel wait (any role)
   kStatusSmemAlign = 7,       // dynamic shared memory base not 1024-byte aligned (kernel did nothing)
+  kStatusSelftest = 8,        // gbattn_selftest_bounded_wait: the wait nothing satisfies gave up
 };
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.

@@ -301,6 +301,19 @@ int gbattn_causal_tile_counts(int Sq, int Sk, int Br, int Bc,
 int gbattn_exp2_paths(const float *x, float *y_poly, float *y_hw, long long n, void *stream);
 
 /*
+ * gbattn_selftest_bounded_wait -- diagnostic of the kernels' failure path:
+ * launches one warp whose thread 0 performs the bounded mbarrier wait every
+ * kernel role uses on its producer (about 2 s limit).  With arrive != 0 the
+ * barrier is satisfied first and nothing is reported; with arrive = 0
+ * nothing ever arrives, the wait gives up without faulting or hanging the
+ * GPU, and the next gbattn_device_status() returns GBATTN_EDEVICE_TIMEOUT.
+ * This is the "consumer waits for a commit the producer never issues" case
+ * of the ring's liveness proof in M4.6 "FlashAttention-3/4 Hardware
+ * Pipelines" 0x03.  Errors: GBATTN_EUNSUPPORTED, GBATTN_ELAUNCH.
+ */
+int gbattn_selftest_bounded_wait(int arrive, void *stream);
+
+/*
  * gbattn_device_status -- read and clear the library's device status word
  * (synchronises the current device).  Returns GBATTN_OK, or
  * GBATTN_EDEVICE_TIMEOUT if a kernel gave up since the last call (a bounded

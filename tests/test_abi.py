@@ -124,6 +124,7 @@ def test_decode_validation(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
 def test_valid_call_without_gpu_is_refused(lib):
     assert _fwd(lib) == -10
+    assert lib.gbattn_selftest_bounded_wait(0, None) == -10
 
 
 def test_causal_tile_planner_matches_page_fixtures(lib, golden):
