@@ -340,36 +340,6 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// ---------------------------------------------------------------- cluster launch control
-// A running CTA asks the hardware to cancel the launch of a CTA of the same
-// grid that has not started yet and to hand over its coordinates (launch
-// order).  The 16-byte answer lands in shared memory and completes 16 bytes
-// of transaction count on `bar` (arm it with mbar_arrive_expect_tx(bar, 16)).
-// After one refused request a CTA must not ask again.
-__device__ __forceinline__ void clc_try_cancel(void* resp16, uint64_t* bar) {
-  asm volatile(
-      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
-          smem_u32(resp16)),
-      "r"(smem_u32(bar))
-      : "memory");
-}
-
-// The x coordinate of the CTA taken over, or -1 if the request was refused.
-__device__ __forceinline__ int clc_taken_ctaid_x(const void* resp16) {
-  uint64_t lo, hi;
-  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(smem_u32(resp16)) : "memory");
-  uint32_t granted, x;
-  asm volatile(
-      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
-      "mov.b128 r, {%2, %3};\n\t"
-      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
-      "selp.b32 %0, 1, 0, p;\n\t"
-      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
-      : "=r"(granted), "=r"(x)
-      : "l"(lo), "l"(hi));
-  return granted ? static_cast<int>(x) : -1;
-}
-
 // ---------------------------------------------------------------- CTA pair
 // Two CTAs of a cluster of two working as one tcgen05 "CTA pair"
 // (cta_group::2): rank 0 issues every MMA; an M = 256 product takes rows
