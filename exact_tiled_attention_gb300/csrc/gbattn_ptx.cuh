@@ -135,16 +135,7 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
-// Bulk (non-tensor) asynchronous reduction: global[dst .. dst+bytes) +=
-// shared[src .. src+bytes) element-wise in fp32.  Both addresses 16-byte
-// aligned, bytes a multiple of 16.  Tracked by the issuing thread's bulk
-// async-group (commit / wait below).
-__device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(gdst)),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
+// Close the group of bulk copies this thread issued since the last commit.
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -153,25 +144,9 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// Wait until every committed bulk group of this thread has completed.
-__device__ __forceinline__ void bulk_wait_group0() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 
-// Named barrier over `nthreads` threads (a multiple of 32) that also returns
-// the AND of `pred` over them; every participating thread must arrive.
-__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred pi, po;\n\t"
-      "setp.ne.u32 pi, %1, 0;\n\t"
-      "barrier.cta.red.and.pred po, %2, %3, pi;\n\t"
-      "selp.u32 %0, 1, 0, po;\n\t}"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
-}
+// Named barrier over `nthreads` threads (a multiple of 32); barrier 0 is
+// __syncthreads.
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -368,10 +343,6 @@ __device__ __forceinline__ uint32_t mapa_shared(const void* p, uint32_t rank) {
   return r;
 }
 
-// Arrive (release, cluster scope) on an mbarrier given by its cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
 
 // Release this thread's shared-memory operations at cluster scope, then
 // arrive (relaxed) on an mbarrier of another CTA.  The fence is restricted to
