@@ -29,6 +29,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -105,9 +106,10 @@ DECODE_SOURCES = ["exact_tiled_attention_gb300/csrc/decode_splitkv.cu",
                   "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]
 
 
-def ncu_traffic(kernel_key: str, sources):
+def ncu_traffic(kernel_key: str, sources, workload: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    kernel source changed since the counters were taken or the record is for
+    another workload (another batch size, say)."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
@@ -116,7 +118,16 @@ def ncu_traffic(kernel_key: str, sources):
     e = d.get(kernel_key)
     if not e or e.get("source_sha") != kernel_source_hash(sources):
         return None
+    if not e.get("workload", "").startswith(workload):
+        return None
     return e.get("dram_bytes_per_launch")
+
+
+def with_batch(w, B: int):
+    """The workload `w` at batch size B, its name carrying the new batch."""
+    import dataclasses
+
+    return dataclasses.replace(w, B=B, name=re.sub(r"_b\d+_", f"_b{B}_", w.name, count=1))
 
 
 class ClockSampler:
@@ -298,7 +309,7 @@ def bench_prefill(args, world, rank, peaks, peak_kind, w=None, with_e2e=True, pa
     key += ("causal>" if w.causal else "noncausal>") + ("" if w is PREFILL else f"@{w.name}")
     if pair:
         key = f"prefill_pair_kernel<{'bf16' if w.dtype == torch.bfloat16 else 'fp16'}>@{w.name}"
-    traffic = ncu_traffic(key, PREFILL_SOURCES)
+    traffic = ncu_traffic(key, PREFILL_SOURCES, w.name)
     dtype_name = "bf16" if w.dtype == torch.bfloat16 else "fp16"
     if not with_e2e:
         return {"workload": w.name, "impl": "cta_pair" if pair else "one_cta", "value": round(tflops_job, 3),
@@ -427,7 +438,7 @@ def bench_decode(args, world, rank, peaks, peak_kind, steps=None, warmup=None):
     gbs_job = nbytes * steps * world / secs / 1e9
     achieved = nbytes / per_step / 1e9
     peak = peaks["hbm_gbs"]
-    traffic = ncu_traffic("decode_partial_kernel<128,bf16>", DECODE_SOURCES)
+    traffic = ncu_traffic("decode_partial_kernel<128,bf16>", DECODE_SOURCES, w.name)
 
     # end to end: only the step's inputs move each step (q and lengths in,
     # O and LSE out); the KV cache is resident state, copied in once before.
@@ -728,11 +739,9 @@ def main():
     world, rank, local = dist_setup()
     peaks, peak_kind = load_peaks()
     if args.batch > 0:
-        import dataclasses
-
         global PREFILL, DECODE
-        PREFILL = dataclasses.replace(PREFILL, B=args.batch)
-        DECODE = dataclasses.replace(DECODE, B=args.batch)
+        PREFILL = with_batch(PREFILL, args.batch)
+        DECODE = with_batch(DECODE, args.batch)
 
     if args.impl == "reference":
         if rank == 0:
@@ -749,9 +758,7 @@ def main():
     if args.fp8_only:
         w2 = PREFILL if args.workload == "prefill" else WORKLOADS[args.workload]
         if args.batch > 0:
-            import dataclasses
-
-            w2 = dataclasses.replace(w2, B=args.batch)
+            w2 = with_batch(w2, args.batch)
         line = bench_fp8(args, world, rank, peaks, peak_kind, w=w2)
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -763,9 +770,7 @@ def main():
     if args.backward_only:
         w2 = PREFILL if args.workload == "prefill" else WORKLOADS[args.workload]
         if args.batch > 0:
-            import dataclasses
-
-            w2 = dataclasses.replace(w2, B=args.batch)
+            w2 = with_batch(w2, args.batch)
         line = bench_backward(args, world, rank, peaks, peak_kind, w=w2)
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -791,9 +796,7 @@ def main():
     elif args.workload in WORKLOADS and not WORKLOADS[args.workload].decode:
         w2 = WORKLOADS[args.workload]
         if args.batch > 0:
-            import dataclasses
-
-            w2 = dataclasses.replace(w2, B=args.batch)
+            w2 = with_batch(w2, args.batch)
         if args.cta_pair:
             line = bench_prefill(args, world, rank, peaks, peak_kind, w=w2, with_e2e=False, pair=True)
         else:
