@@ -486,13 +486,14 @@ def bench_decode(args, world, rank, peaks, peak_kind, steps=None, warmup=None):
     }
 
 
-def bench_backward(args, world, rank, peaks, peak_kind, w=None, steps=None, warmup=None):
-    """attn_bwd on a forward workload: O and LSE from one attn_fwd call (not
-    timed), then preprocess + main + dQ conversion timed per step.  FLOPs:
-    the pages' convention of 2.5x the forward (five matmul-shaped products
-    instead of two), i.e. 10*B*H*Sq*Sk*d, halved for causal."""
-    from exact_tiled_attention_gb300 import (attn_bwd, attn_bwd_workspace_bytes, attn_fwd,
-                                             gbattn_device_status)
+def bench_backward(args, world, rank, peaks, peak_kind, w=None, steps=None, warmup=None, atomic=False):
+    """attn_bwd (or, with atomic, attn_bwd_atomic) on a forward workload: O and
+    LSE from one attn_fwd call (not timed), then the backward's three kernels
+    timed per step.  FLOPs: the pages' convention of 2.5x the forward (five
+    matmul-shaped products instead of two), i.e. 10*B*H*Sq*Sk*d, halved for
+    causal."""
+    from exact_tiled_attention_gb300 import (attn_bwd, attn_bwd_atomic, attn_bwd_atomic_workspace_bytes,
+                                             attn_bwd_workspace_bytes, attn_fwd, gbattn_device_status)
     from exact_tiled_attention_gb300.inputs import make_generator, randn
 
     w = w or PREFILL
@@ -503,9 +504,10 @@ def bench_backward(args, world, rank, peaks, peak_kind, w=None, steps=None, warm
     do = randn(q.shape, q.dtype, make_generator(w.seed + 100, "cuda"), "cuda")
     o, lse = attn_fwd(q, k, v, scale=w.scale, causal=w.causal, stream=stream)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(attn_bwd_workspace_bytes(w.B, w.H, w.Sq, w.d), dtype=torch.uint8, device="cuda")
-    run = lambda: attn_bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, workspace=ws,  # noqa: E731
-                           dq=dq, dk=dk, dv=dv, stream=stream)
+    ws_fn, fn = (attn_bwd_atomic_workspace_bytes, attn_bwd_atomic) if atomic else (attn_bwd_workspace_bytes, attn_bwd)
+    ws = torch.empty(ws_fn(w.B, w.H, w.Sq, w.d), dtype=torch.uint8, device="cuda")
+    run = lambda: fn(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, workspace=ws,  # noqa: E731
+                     dq=dq, dk=dk, dv=dv, stream=stream)
     footprint = 9 * q.numel() * 2 + ws.numel()
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
@@ -526,6 +528,7 @@ def bench_backward(args, world, rank, peaks, peak_kind, w=None, steps=None, warm
     achieved = flops / per_call / 1e12
     peak = peaks["bf16_tflops"]
     return {"metric": "attention bwd TFLOP/s (% BF16 tensor peak)", "workload": w.name,
+            "impl": "atomic_dq (attn_bwd_atomic)" if atomic else "two_owner (attn_bwd)",
             "value": round(flops * steps * world / secs / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_call": round(per_call * 1e3, 4), "steps": steps, "warmup": warmup,
             "flops_per_call": flops, "flop_convention": "2.5 x forward (10*B*H*Sq*Sk*d, /2 causal)",
@@ -723,6 +726,8 @@ def main():
                     choices=["prefill", "decode"] + [n for n, w in WORKLOADS.items() if not w.decode])
     ap.add_argument("--fp8-only", action="store_true",
                     help="time only attn_fwd_fp8 on the headline forward workload (profiling runs)")
+    ap.add_argument("--atomic", action="store_true",
+                    help="with --backward-only: time attn_bwd_atomic instead of attn_bwd")
     ap.add_argument("--backward-only", action="store_true",
                     help="time only attn_bwd on the headline forward workload (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -771,7 +776,7 @@ def main():
         w2 = PREFILL if args.workload == "prefill" else WORKLOADS[args.workload]
         if args.batch > 0:
             w2 = with_batch(w2, args.batch)
-        line = bench_backward(args, world, rank, peaks, peak_kind, w=w2)
+        line = bench_backward(args, world, rank, peaks, peak_kind, w=w2, atomic=args.atomic)
         if rank == 0:
             print(json.dumps(line), flush=True)
         if world > 1:
@@ -793,6 +798,8 @@ def main():
             bw_steps = max(3, min(args.steps, 20))
             line["backward"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
                                                warmup=3) for w2 in BACKWARD]
+            line["backward_atomic"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
+                                                      warmup=3, atomic=True) for w2 in BACKWARD if w2.d == 128]
     elif args.workload in WORKLOADS and not WORKLOADS[args.workload].decode:
         w2 = WORKLOADS[args.workload]
         if args.batch > 0:

@@ -10,6 +10,8 @@ from .binding import (  # noqa: F401
     GbattnError,
     LIB_PATH,
     attn_bwd,
+    attn_bwd_atomic,
+    attn_bwd_atomic_workspace_bytes,
     attn_bwd_workspace_bytes,
     attn_decode_splitkv,
     attn_decode_splitkv_noalloc,

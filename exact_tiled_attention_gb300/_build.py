@@ -23,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgbattn.so")
 
 SOURCES = ["gbattn_api.cu", "prefill_fwd.cu", "prefill_pair.cu", "prefill_fp8.cu", "decode_splitkv.cu",
-           "decode_noalloc.cu", "backward.cu"]
+           "decode_noalloc.cu", "backward.cu", "backward_atomic.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

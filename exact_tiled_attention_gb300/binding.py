@@ -29,7 +29,8 @@ ERRORS = {
 }
 EXPORTS = ("attn_fwd", "attn_fwd_pair", "attn_decode_workspace_bytes", "attn_decode_splitkv",
            "attn_decode_splitkv_noalloc", "attn_decode_noalloc_scratch_bytes",
-           "attn_bwd_workspace_bytes", "attn_bwd", "gbattn_exp2_paths",
+           "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_atomic_workspace_bytes", "attn_bwd_atomic",
+           "gbattn_exp2_paths",
            "attn_fwd_fp8_workspace_bytes", "attn_fwd_fp8", "gbattn_selftest_bounded_wait",
            "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_error_string",
            "gbattn_version")
@@ -76,6 +77,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp,
                                  sz, ci, vp]
         lib.attn_bwd.restype = ci
+        lib.attn_bwd_atomic_workspace_bytes.argtypes = [ci, ci, ci, ci]
+        lib.attn_bwd_atomic_workspace_bytes.restype = sz
+        lib.attn_bwd_atomic.argtypes = lib.attn_bwd.argtypes
+        lib.attn_bwd_atomic.restype = ci
         lib.attn_fwd_fp8_workspace_bytes.argtypes = [ci, ci, ci, ci]
         lib.attn_fwd_fp8_workspace_bytes.restype = sz
         lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cf, ci, vp, sz, vp]
@@ -315,12 +320,32 @@ def attn_bwd_workspace_bytes(B: int, H: int, Sq: int, d: int) -> int:
 
 def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
              workspace=None, dq=None, dk=None, dv=None, stream=None):
-    """Exact attention backward through the C ABI `attn_bwd`.
+    """Exact attention backward through the C ABI `attn_bwd` (two owners, no
+    atomics: bitwise repeatable).
 
     q, o, dout [B,H,Sq,d]; k, v [B,Hkv,Sk,d] (fp16/bf16, CUDA, contiguous);
     lse [B,H,Sq] fp32 from attn_fwd.  workspace: optional caller-owned CUDA
     buffer of at least attn_bwd_workspace_bytes(B, H, Sq, d) bytes (allocated
     here if omitted).  Returns (dq, dk, dv)."""
+    return _bwd_call("attn_bwd", "attn_bwd_workspace_bytes", q, k, v, o, lse, dout, scale, causal,
+                     workspace, dq, dk, dv, stream)
+
+
+def attn_bwd_atomic_workspace_bytes(B: int, H: int, Sq: int, d: int) -> int:
+    return int(load_library().attn_bwd_atomic_workspace_bytes(B, H, Sq, d))
+
+
+def attn_bwd_atomic(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
+                    workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Exact attention backward through the C ABI `attn_bwd_atomic`: one
+    owner per key tile, dQ summed by fp32 atomic adds (not bitwise
+    repeatable in dQ).  Head dimension 128.  Arguments and result as attn_bwd;
+    the workspace is attn_bwd_atomic_workspace_bytes(B, H, Sq, d) bytes."""
+    return _bwd_call("attn_bwd_atomic", "attn_bwd_atomic_workspace_bytes", q, k, v, o, lse, dout, scale,
+                     causal, workspace, dq, dk, dv, stream)
+
+
+def _bwd_call(fn, ws_fn, q, k, v, o, lse, dout, scale, causal, workspace, dq, dk, dv, stream):
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
         _check(t, n, 4)
     B, H, Sq, d = q.shape
@@ -336,19 +361,19 @@ def attn_bwd(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = F
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     lib = load_library()
-    need = int(lib.attn_bwd_workspace_bytes(B, H, Sq, d))
+    need = int(getattr(lib, ws_fn)(B, H, Sq, d))
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    rc = lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                      dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, Sq, Sk,
-                      d, float(scale), int(bool(causal)), workspace.data_ptr(), ws_bytes, dt,
-                      _stream_ptr(stream))
+    rc = getattr(lib, fn)(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                          dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, Sq, Sk,
+                          d, float(scale), int(bool(causal)), workspace.data_ptr(), ws_bytes, dt,
+                          _stream_ptr(stream))
     if rc != GBATTN_OK:
-        raise GbattnError(rc, "attn_bwd")
+        raise GbattnError(rc, fn)
     return dq, dk, dv
 
 

@@ -289,6 +289,57 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   return launch_backward(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
+size_t attn_bwd_atomic_workspace_bytes(int B, int H, int Sq, int d) {
+  const size_t dbytes = attn_bwd_workspace_bytes(B, H, Sq, d);
+  if (dbytes == 0) return 0;
+  // the row scalars D, then the fp32 dQ accumulator [B, H, Sq, d]
+  return dbytes + static_cast<size_t>(B) * H * Sq * d * sizeof(float);
+}
+
+int attn_bwd_atomic(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int Sq, int Sk,
+                    int d, float scale, int causal, void* workspace, size_t workspace_bytes, int dtype,
+                    void* stream) {
+  if (B < 1 || H < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return GBATTN_EBADSHAPE;
+  if (H % Hkv != 0) return GBATTN_EHEADS;
+  if (d != 128) return GBATTN_EHEADDIM;
+  if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
+  const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs)
+    if (!ptr || !aligned16(ptr)) return GBATTN_EPOINTER;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return GBATTN_EPOINTER;
+  if (static_cast<long long>(B) * H > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
+    return GBATTN_EBADSHAPE;
+  if (workspace_bytes < attn_bwd_atomic_workspace_bytes(B, H, Sq, d)) return GBATTN_EWORKSPACE;
+  int* status = nullptr;
+  int rc = current_device(&status);
+  if (rc != GBATTN_OK) return rc;
+  BackwardArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.H = H;
+  a.Hkv = Hkv;
+  a.Sq = Sq;
+  a.Sk = Sk;
+  a.d = d;
+  a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  a.Dvec = static_cast<float*>(workspace);
+  a.dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + attn_bwd_workspace_bytes(B, H, Sq, d));
+  a.bf16 = dtype == GBATTN_BF16;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.status = status;
+  return launch_backward_atomic(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
 size_t attn_fwd_fp8_workspace_bytes(int B, int Hkv, int Sk, int d) {
   if (B < 1 || Hkv < 1 || Sk < 1 || d < 1) return 0;
   const size_t sk_pad = (static_cast<size_t>(Sk) + 127) / 128 * 128;

@@ -56,6 +56,7 @@ struct BackwardArgs {
   float scale;
   int causal;
   float* Dvec;    // workspace: [B*H*Sq] fp32 row scalars D
+  float* dq_acc = nullptr;  // atomic variant: workspace [B*H*Sq*d] fp32 dQ accumulator
   bool bf16;
   cudaStream_t stream;
   int* status;
@@ -87,6 +88,9 @@ int launch_prefill(const PrefillArgs& a);
 int launch_prefill_pair(const PrefillArgs& a);
 int launch_decode(const DecodeArgs& a);
 int launch_backward(const BackwardArgs& a);
+// Column owner with fp32 atomic dQ (backward_atomic.cu); d = 128 and a.dq_acc
+// set, else -1.
+int launch_backward_atomic(const BackwardArgs& a);
 int launch_prefill_fp8(const PrefillFp8Args& a);
 
 // cuTensorMapEncodeTiled fetched once through the runtime's driver entry

@@ -242,6 +242,37 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
              void *workspace, size_t workspace_bytes, int dtype, void *stream);
 
 /*
+ * attn_bwd_atomic_workspace_bytes -- bytes of device workspace attn_bwd_atomic
+ * needs: attn_bwd_workspace_bytes(B, H, Sq, d) for the fp32 row scalars D,
+ * then the fp32 dQ accumulator [B, H, Sq, d] (the dQaccum entry of the
+ * scratch ledger in M4.4 0x06.1J).  Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_atomic_workspace_bytes(int B, int H, int Sq, int d);
+
+/*
+ * attn_bwd_atomic -- exact attention backward on the schedule of M4.4
+ * 0x06.1D: one CTA per (128-key tile, batch, KV head) owns dK and dV (summed
+ * over the H/Hkv query heads of the group in its accumulators, 0x06.1H) and
+ * adds every query block's contribution dS_ij K_j into the fp32 dQ
+ * accumulator with atomic adds; a last kernel writes dQ = scale * accumulator
+ * in the input dtype.  Same arguments, layouts and definition as attn_bwd
+ * (d must be 128); workspace is caller-owned device scratch of at least
+ * attn_bwd_atomic_workspace_bytes(B, H, Sq, d) bytes, 16-byte aligned, its
+ * contents on entry irrelevant (the call zeroes the accumulator).
+ *
+ * Atomic adds reach every contribution but not in a fixed order (0x06.1F),
+ * so dQ may differ in its last bits between calls; dK and dV are bitwise
+ * repeatable.  Five 128 x 128 products per (query block, key tile) pair
+ * against attn_bwd's seven.
+ *
+ * Errors: as attn_bwd; GBATTN_EHEADDIM for d != 128.
+ */
+int attn_bwd_atomic(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                    const void *dout, void *dq, void *dk, void *dv,
+                    int B, int H, int Hkv, int Sq, int Sk, int d, float scale, int causal,
+                    void *workspace, size_t workspace_bytes, int dtype, void *stream);
+
+/*
  * attn_decode_splitkv_noalloc -- attn_decode_splitkv for callers that cannot
  * allocate device memory (a host framework that owns every allocation and
  * forbids plugins from calling cudaMalloc, memory-capped or real-time

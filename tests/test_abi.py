@@ -184,3 +184,40 @@ def test_bwd_validation(lib):
     assert _bwd(lib, lse=FAKE + 2) == -5
     need = lib.attn_bwd_workspace_bytes(1, 4, 8, 128)
     assert _bwd(lib, wsb=need - 1) == -6
+
+
+def _bwd_atomic(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, do=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, B=1, H=4,
+             Hkv=2, Sq=8, Sk=8, d=128, scale=0.1, causal=1, ws=FAKE, wsb=1 << 20, dtype=1, stream=None)
+    a.update(kw)
+    return lib.attn_bwd_atomic(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"], a["dv"],
+                               a["B"], a["H"], a["Hkv"], a["Sq"], a["Sk"], a["d"], a["scale"], a["causal"],
+                               a["ws"], a["wsb"], a["dtype"], a["stream"])
+
+
+def test_bwd_atomic_workspace_matches_page_ledger(lib, golden):
+    """The atomic backward's workspace is the ledger's D plus its fp32
+    dQaccum (M4.4 0x06.1J): 64.5 MiB at the ledger coordinate; no expanded
+    dK/dV (the grouped sum happens in the key-tile owner's accumulators)."""
+    g = golden("bwd_scratch_ledger.json")
+    c = g["coordinate"]
+    mib = 1 << 20
+    want = (g["objects_mib"]["D"] + g["objects_mib"]["dQaccum"]) * mib
+    assert lib.attn_bwd_atomic_workspace_bytes(c["B"], c["Hq"], c["Sq"], c["d"]) == want
+    assert lib.attn_bwd_atomic_workspace_bytes(0, 1, 1, 128) == 0
+
+
+def test_bwd_atomic_validation(lib):
+    assert _bwd_atomic(lib, B=0) == -1
+    assert _bwd_atomic(lib, Sk=0) == -1
+    assert _bwd_atomic(lib, H=6, Hkv=4) == -2
+    assert _bwd_atomic(lib, d=64) == -3
+    assert _bwd_atomic(lib, d=96) == -3
+    assert _bwd_atomic(lib, dtype=2) == -4
+    for name in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv", "ws"):
+        assert _bwd_atomic(lib, **{name: None}) == -5, name
+    assert _bwd_atomic(lib, dq=FAKE + 8) == -5
+    assert _bwd_atomic(lib, lse=FAKE + 2) == -5
+    need = lib.attn_bwd_atomic_workspace_bytes(1, 4, 8, 128)
+    assert need == 256 + 4 * 8 * 128 * 4
+    assert _bwd_atomic(lib, wsb=need - 1) == -6

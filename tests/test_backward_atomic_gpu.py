@@ -1,0 +1,133 @@
+"""GPU parity of the atomic-dQ backward (C ABI attn_bwd_atomic) against the
+fp64 oracle, plus its contract: dK and dV repeat bitwise, dQ agrees with the
+two-owner backward to rounding, d = 64 and short workspaces are refused."""
+import math
+
+import pytest
+import torch
+
+import oracle
+from exact_tiled_attention_gb300 import (GbattnError, attn_bwd, attn_bwd_atomic, attn_bwd_atomic_workspace_bytes,
+                                         attn_fwd, gbattn_device_status)
+from exact_tiled_attention_gb300.inputs import WORKLOADS, make_generator, make_prefill, randn
+from tests.parity_util import assert_grad_close, host_f32
+
+pytestmark = pytest.mark.gpu
+
+DT = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+def _fwd_bwd(q, k, v, do, scale, causal):
+    o, lse = attn_fwd(q, k, v, scale=scale, causal=causal)
+    dq, dk, dv = attn_bwd_atomic(q, k, v, o, lse, do, scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    assert gbattn_device_status() == 0
+    return dq, dk, dv
+
+
+def _dout(shape, dtype, seed):
+    return randn(shape, dtype, make_generator(seed, "cuda"), "cuda")
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 1, 128, 128, "bf16", False),
+    (1, 2, 2, 300, 300, "bf16", True),     # ragged tails, diagonal blocks
+    (1, 2, 2, 300, 300, "fp16", False),
+    (2, 4, 2, 257, 257, "bf16", True),     # GQA g = 2
+    (1, 2, 2, 129, 700, "fp16", False),    # Sq != Sk
+    (1, 4, 1, 512, 512, "bf16", True),     # MQA g = 4
+    (1, 2, 2, 64, 1000, "bf16", True),     # causal Sq < Sk (bottom-right)
+    (1, 2, 1, 200, 77, "bf16", True),      # causal Sq > Sk: rows with no key
+    (1, 1, 1, 1, 1, "bf16", False),
+    (2, 2, 2, 1, 333, "fp16", True),
+    (1, 2, 2, 333, 1, "bf16", False),
+    (1, 2, 2, 1024, 1024, "bf16", False),  # several query blocks per key tile
+])
+def test_bwd_atomic_small_all_elements(shape):
+    B, H, Hkv, Sq, Sk, dt, causal = shape
+    d = 128
+    q, k, v = make_prefill(B, H, Hkv, Sq, Sk, d, DT[dt], 31, device="cuda")
+    do = _dout((B, H, Sq, d), DT[dt], 32)
+    scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = _fwd_bwd(q, k, v, do, scale, causal)
+    rq, rk, rv, _, _ = oracle.attn_bwd(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, causal)
+    assert_grad_close(dq, rq, f"dq {shape}")
+    assert_grad_close(dk, rk, f"dk {shape}")
+    assert_grad_close(dv, rv, f"dv {shape}")
+
+
+@pytest.mark.parametrize("scale", [0.05, 0.9])
+def test_bwd_atomic_scales(scale):
+    q, k, v = make_prefill(1, 4, 2, 260, 300, 128, torch.bfloat16, 43, device="cuda")
+    do = _dout(q.shape, torch.bfloat16, 44)
+    dq, dk, dv = _fwd_bwd(q, k, v, do, scale, True)
+    rq, rk, rv, _, _ = oracle.attn_bwd(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, True)
+    assert_grad_close(dq, rq, f"dq scale {scale}")
+    assert_grad_close(dk, rk, f"dk scale {scale}")
+    assert_grad_close(dv, rv, f"dv scale {scale}")
+
+
+@pytest.mark.parametrize("name,kv_ids", [
+    ("causal_bf16_b4_h16_s8192_d128", [0, 63]),
+    ("gqa_causal_bf16_b2_hq32_hkv8_s4096_d128", [1, 14]),
+])
+def test_bwd_atomic_workload_sampled_heads(name, kv_ids):
+    w = WORKLOADS[name]
+    q, k, v = make_prefill(w.B, w.H, w.Hkv, w.Sq, w.Sk, w.d, w.dtype, w.seed, device="cuda")
+    do = _dout((w.B, w.H, w.Sq, w.d), w.dtype, w.seed + 100)
+    dq, dk, dv = _fwd_bwd(q, k, v, do, w.scale, w.causal)
+    assert torch.isfinite(dq).all() and torch.isfinite(dk).all() and torch.isfinite(dv).all()
+    g = w.H // w.Hkv
+    rq, rk, rv = oracle.attn_bwd_kvheads(host_f32(q), host_f32(k), host_f32(v), host_f32(do), w.scale,
+                                         w.causal, kv_ids)
+    for r, kid in enumerate(kv_ids):
+        b, kvh = divmod(kid, w.Hkv)
+        assert_grad_close(dq[b, kvh * g:(kvh + 1) * g], rq[r], f"{name} dq kv{kid}")
+        assert_grad_close(dk[b, kvh], rk[r], f"{name} dk kv{kid}")
+        assert_grad_close(dv[b, kvh], rv[r], f"{name} dv kv{kid}")
+
+
+def test_bwd_atomic_repeatability_and_agreement():
+    """dK and dV have one writer each: identical bits on every call.  dQ sums
+    its key tiles in arrival order: calls agree to fp32 rounding of the
+    accumulator, and with the two-owner backward to the dtype's rounding."""
+    q, k, v = make_prefill(1, 4, 2, 1500, 1500, 128, torch.bfloat16, 51, device="cuda")
+    do = _dout(q.shape, torch.bfloat16, 52)
+    o, lse = attn_fwd(q, k, v, causal=True)
+    a = attn_bwd_atomic(q, k, v, o, lse, do, causal=True)
+    b = attn_bwd_atomic(q, k, v, o, lse, do, causal=True)
+    ref = attn_bwd(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    assert gbattn_device_status() == 0
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    scale_q = a[0].float().abs().max().item()
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2 * scale_q
+    for x, y, n in zip(a, ref, ("dq", "dk", "dv")):
+        err = (x.float() - y.float()).abs().max().item()
+        assert err <= 2e-2 * y.float().abs().max().item(), n
+
+
+def test_bwd_atomic_key_gradient_sums_to_zero():
+    """sum_j dK_j = 0 per KV head (rows of dS sum to zero) at any size."""
+    B, H, Hkv, S, d = 1, 4, 2, 1000, 128
+    q, k, v = make_prefill(B, H, Hkv, S, S, d, torch.bfloat16, 41, device="cuda")
+    do = _dout((B, H, S, d), torch.bfloat16, 42)
+    dq, dk, dv = _fwd_bwd(q, k, v, do, 1 / math.sqrt(d), True)
+    col = dk.double().sum(dim=2)
+    assert (col.abs().max() / dk.double().abs().max()).item() <= 5e-2
+
+
+def test_bwd_atomic_refusals():
+    q, k, v = make_prefill(1, 2, 2, 100, 100, 64, torch.bfloat16, 61, device="cuda")
+    o, lse = attn_fwd(q, k, v)
+    with pytest.raises(GbattnError, match="EHEADDIM"):
+        attn_bwd_atomic(q, k, v, o, lse, q)
+    q, k, v = make_prefill(1, 2, 2, 100, 100, 128, torch.bfloat16, 62, device="cuda")
+    o, lse = attn_fwd(q, k, v)
+    need = attn_bwd_atomic_workspace_bytes(1, 2, 100, 128)
+    assert need == 256 * ((1 * 2 * 100 * 4 + 255) // 256) + 2 * 100 * 128 * 4
+    short = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(GbattnError, match="EWORKSPACE"):
+        attn_bwd_atomic(q, k, v, o, lse, q, workspace=short)
+    torch.cuda.synchronize()
+    assert gbattn_device_status() == 0
