@@ -799,7 +799,7 @@ def main():
             line["backward"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
                                                warmup=3) for w2 in BACKWARD]
             line["backward_atomic"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
-                                                      warmup=3, atomic=True) for w2 in BACKWARD if w2.d == 128]
+                                                      warmup=3, atomic=True) for w2 in BACKWARD]
     elif args.workload in WORKLOADS and not WORKLOADS[args.workload].decode:
         w2 = WORKLOADS[args.workload]
         if args.batch > 0:

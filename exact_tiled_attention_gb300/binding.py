@@ -339,7 +339,7 @@ def attn_bwd_atomic(q, k, v, o, lse, dout, scale: float | None = None, causal: b
                     workspace=None, dq=None, dk=None, dv=None, stream=None):
     """Exact attention backward through the C ABI `attn_bwd_atomic`: one
     owner per key tile, dQ summed by fp32 atomic adds (not bitwise
-    repeatable in dQ).  Head dimension 128.  Arguments and result as attn_bwd;
+    repeatable in dQ).  Head dimension 64 or 128.  Arguments and result as attn_bwd;
     the workspace is attn_bwd_atomic_workspace_bytes(B, H, Sq, d) bytes."""
     return _bwd_call("attn_bwd_atomic", "attn_bwd_atomic_workspace_bytes", q, k, v, o, lse, dout, scale,
                      causal, workspace, dq, dk, dv, stream)

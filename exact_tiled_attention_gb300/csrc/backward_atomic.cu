@@ -63,6 +63,9 @@ constexpr int kDrainWarp0 = 12;  // warps 12-15: dQ^T drain
 // a dQ^T row in registers).
 constexpr int kRegsCompute = 136, kRegsCtl = 88, kRegsDrain = 152;
 static_assert(2 * 128 * kRegsCompute + 128 * kRegsCtl + 128 * kRegsDrain <= kThreads * 128, "register split");
+// setmaxnreg.inc may only raise a warp's count and .dec only lower it (the
+// launch gives 128 a thread): the roles below use inc / dec accordingly.
+static_assert(kRegsCompute >= 128 && kRegsDrain >= 128 && kRegsCtl <= 128, "inc / dec directions");
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int kBlock = kT * 128;       // 16 KiB: 128 rows x one 128-byte (64-element) column block
@@ -546,21 +549,483 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarpX) tmem_dealloc(tmem, 512);
 }
 
+// =========================================================================
+// Head dimension 64.  The same schedule; tensor memory and shared memory now
+// have room to spare, so dQ (= dS K: query rows on the TMEM lane axis, 64
+// head-dim columns) gets columns of its own and dP^T(t+1) no longer waits for
+// the drain, and each drain warp stages its 32 query rows of dQ in shared
+// memory and adds them into the accumulator with two TMA bulk tensor
+// reductions (off the load/store queue the compute warpgroups use).
+//   dQ = dS K      A = dS (the dS^T tile read MN-major), B = K (MN-major)
+//   TMEM: dV [0,64), dK [64,128), S^T/P^T [128,256), dP^T [256,384), dQ [384,448).
+// =========================================================================
+namespace d64 {
+constexpr int kD = 64;
+constexpr int kTile = kT * kD * 2;  // 16 KiB: 128 rows x 64 elements, one column block
+constexpr int kStages = 3;          // Q/dO stages
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTile;
+constexpr int kOffQ = kOffV + kTile;
+constexpr int kOffDO = kOffQ + kStages * kTile;
+constexpr int kOffPS = kOffDO + kStages * kTile;  // dS^T: 128 keys x 128 queries, two column blocks
+constexpr int kOffStage = kOffPS + 2 * kBlock;    // dQ staging: per drain warp two 32-row x 32-float boxes
+constexpr int kBoxBytes = 32 * 128;               // 4 KiB
+constexpr int kOffStats = kOffStage + 8 * kBoxBytes;
+constexpr int kOffBars = kOffStats + kStages * 2 * kT * 4;
+constexpr int kSmemBytes = kOffBars + 256;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kColDV = 0, kColDK = 64, kColX = 128, kColY = 256, kColQ = 384;
+constexpr int kRegsCompute = 160, kRegsCtl = 88, kRegsDrain = 104;
+static_assert(2 * 128 * kRegsCompute + 128 * kRegsCtl + 128 * kRegsDrain <= kThreads * 128, "register split");
+// directions from the launch's 128: compute inc, control and drain dec
+static_assert(kRegsCompute >= 128 && kRegsCtl <= 128 && kRegsDrain <= 128, "inc / dec directions");
+
+struct __align__(8) Bars {
+  uint64_t kv_full;
+  uint64_t qd_full[kStages];
+  uint64_t qd_empty[kStages];
+  uint64_t s_full, dp_full, dp_free;
+  uint64_t p_full, ds_full;
+  uint64_t dv_done, dk_done;
+  uint64_t dq_full, dq_free;
+  uint64_t acc_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+}  // namespace d64
+
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_atomic64_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                        const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                        const __grid_constant__ CUtensorMap tmap_dq, const AtomicParams p) {
+  // this kernel's layout (shadows the 128-dim constants)
+  constexpr int kD = d64::kD, kTile = d64::kTile, kStages = d64::kStages;
+  constexpr int kOffK = d64::kOffK, kOffV = d64::kOffV, kOffQ = d64::kOffQ, kOffDO = d64::kOffDO;
+  constexpr int kOffPS = d64::kOffPS, kOffStage = d64::kOffStage, kBoxBytes = d64::kBoxBytes;
+  constexpr int kOffStats = d64::kOffStats, kOffBars = d64::kOffBars;
+  constexpr uint32_t kColDV = d64::kColDV, kColDK = d64::kColDK, kColX = d64::kColX, kColY = d64::kColY,
+                     kColQ = d64::kColQ;
+  constexpr int kRegsCompute = d64::kRegsCompute, kRegsCtl = d64::kRegsCtl, kRegsDrain = d64::kRegsDrain;
+  using Bars64 = d64::Bars;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {  // uniform over the CTA
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kStatusSmemAlign);
+    return;
+  }
+  Bars64* bars = reinterpret_cast<Bars64*>(smem + kOffBars);
+  float* stats = reinterpret_cast<float*>(smem + kOffStats);  // [stage][lse2 128 | D 128]
+  volatile int* abort_flag = &bars->abort_flag;
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- work unit: as the 128-dim kernel
+  const int BHkv = p.B * p.Hkv;
+  const int group = blockIdx.x / (p.head_group * p.n_ktiles);
+  const int heads_here = min(p.head_group, BHkv - group * p.head_group);
+  const int r_in = blockIdx.x - group * p.head_group * p.n_ktiles;
+  const int bkv = group * p.head_group + r_in % heads_here;
+  const int jt = r_in / heads_here;
+  const int b = bkv / p.Hkv;
+  const int kvh = bkv % p.Hkv;
+  const int k0 = jt * kT;
+  const int nqb = p.n_qtiles;
+  int i_start = 0;
+  if (CAUSAL) {
+    const int q_min = k0 - p.delta;
+    i_start = q_min <= 0 ? 0 : (q_min >= p.Sq ? nqb : q_min / kT);
+  }
+  const int n_blk = nqb - i_start;
+  const int T = p.g * n_blk;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->kv_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars->qd_full[s], 1 + 32);  // TMA arrive + 32 lanes' stat stores
+      mbar_init(&bars->qd_empty[s], 2);      // released by both issuers
+    }
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->dp_full, 1);
+    mbar_init(&bars->dp_free, 256);
+    mbar_init(&bars->p_full, 256);
+    mbar_init(&bars->ds_full, 256);
+    mbar_init(&bars->dv_done, 1);
+    mbar_init(&bars->dk_done, 1);
+    mbar_init(&bars->dq_full, 1);
+    mbar_init(&bars->dq_free, 128);
+    mbar_init(&bars->acc_done, 2);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
+    prefetch_tensormap(&tmap_do);
+  }
+  if (warp == kDrainWarp0 && lane == 0) prefetch_tensormap(&tmap_dq);
+  if (warp == kMmaWarpX) {
+    tmem_alloc(&bars->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  auto block_coords = [&](int t, int& h, int& q0) {
+    const int hh = t / n_blk;
+    h = kvh * p.g + hh;
+    q0 = (i_start + (t - hh * n_blk)) * kT;
+  };
+
+  if (warp >= kDrainWarp0) {
+    // ================================================================ dQ drain
+    // Warp w owns query rows [32 (w % 4), +32) of the block: dQ rows ->
+    // registers -> columns released -> its two swizzled 32 x 32 fp32 boxes
+    // -> two TMA reduce-adds into the accumulator.
+    regs_dec<kRegsDrain>();  // below the launch's 128: setmaxnreg.inc may only raise the count
+    const int wq = warp % 4;
+    const uint32_t col = tmem + (static_cast<uint32_t>(wq * 32) << 16) + kColQ;
+    uint8_t* stage = smem + kOffStage + wq * 2 * kBoxBytes;
+    for (int t = 0; t < T; ++t) {
+      const bool ok = wait_bar(&bars->dq_full, t & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      uint32_t w[2][32];
+      tmem_ld32(col, w[0]);
+      tmem_ld32(col + 32, w[1]);
+      tmem_wait_ld();
+      reg_fence32(w[0]);
+      reg_fence32(w[1]);
+      tc_fence_before();
+      mbar_arrive(&bars->dq_free);
+      int h, q0;
+      block_coords(t, h, q0);
+      const int y = q0 + 32 * wq;
+      if (lane == 0 && t > 0) bulk_wait_group_read0();  // this warp's previous boxes are read
+      __syncwarp();
+      // row `lane` of box j (head-dim columns [32 j, 32 j + 32)): 16-byte chunk c at c ^ (lane % 8)
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<uint4*>(stage + j * kBoxBytes + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+              make_uint4(w[j][4 * c], w[j][4 * c + 1], w[j][4 * c + 2], w[j][4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0 && y < p.Sq) {
+        tma_reduce_add_3d(&tmap_dq, stage, 0, y, b * p.H + h);
+        tma_reduce_add_3d(&tmap_dq, stage + kBoxBytes, 32, y, b * p.H + h);
+        bulk_commit_group();
+      }
+    }
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+  } else if (warp >= kLoadWarp) {
+    regs_dec<kRegsCtl>();
+    if (warp == kLoadWarp && T > 0) {
+      // ============================================================== loader
+      const uint64_t once = policy_evict_first();
+      const uint64_t reuse = policy_evict_last();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars->kv_full, 2 * kTile);
+        tma_load_3d(smem + kOffK, &tmap_k, &bars->kv_full, 0, k0, bkv, once);
+        tma_load_3d(smem + kOffV, &tmap_v, &bars->kv_full, 0, k0, bkv, once);
+      }
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int s = t % kStages;
+        const bool ok = wait_bar(&bars->qd_empty[s], ((t / kStages) & 1) ^ 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        int h, q0;
+        block_coords(t, h, q0);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->qd_full[s], 2 * kTile);
+          tma_load_3d(smem + kOffQ + s * kTile, &tmap_q, &bars->qd_full[s], 0, q0, b * p.H + h, reuse);
+          tma_load_3d(smem + kOffDO + s * kTile, &tmap_do, &bars->qd_full[s], 0, q0, b * p.H + h, reuse);
+        }
+        const long long row0 = (static_cast<long long>(b) * p.H + h) * p.Sq;
+        float* st = stats + s * 2 * kT;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = lane + 32 * u;
+          const int row = q0 + c;
+          float l2 = INFINITY, dv = 0.f;
+          if (row < p.Sq) {
+            const float lse = p.lse[row0 + row];
+            if (lse != -INFINITY) l2 = lse * kLog2e;
+            dv = p.Dvec[row0 + row];
+          }
+          st[c] = l2;
+          st[kT + c] = dv;
+        }
+        mbar_arrive(&bars->qd_full[s]);
+        issued = t + 1;
+      }
+      if (lane == 0) {
+        int dummy = 0;
+        volatile int* no_abort = reinterpret_cast<volatile int*>(&dummy);
+        bounded_wait(&bars->kv_full, 0, no_abort, p.status, kStatusTimeoutDrain);
+        for (int t = max(0, issued - kStages); t < issued; ++t)
+          bounded_wait(&bars->qd_full[t % kStages], (t / kStages) & 1, no_abort, p.status, kStatusTimeoutDrain);
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarpX || warp == kMmaWarpY) {
+      // ============================================================== MMA issuers
+      //   X: dV(t) once P^T(t) is written; S^T(t+1) once dV(t) has read it.
+      //   Y: dP^T(t+1) once dP^T(t) is in registers; dQ(t), dK(t) once dS^T(t)
+      //      is in shared memory (dQ(t) also once dQ(t-1) is drained).
+      const bool chain_x = warp == kMmaWarpX;
+      if (lane == 0 && T > 0) {
+        constexpr uint32_t kIdS = idesc_f16(BF16, false, false, 128, 128);  // S^T, dP^T
+        constexpr uint32_t kIdAcc = idesc_f16(BF16, false, true, 128, kD);  // dV (TS), dK (SS)
+        constexpr uint32_t kIdDQ = idesc_f16(BF16, true, true, 128, kD);    // dQ: both MN-major
+        const uint64_t k_kmaj = smem_desc_sw128(smem_u32(smem + kOffK), 16, 1024);
+        const uint64_t v_kmaj = smem_desc_sw128(smem_u32(smem + kOffV), 16, 1024);
+        const uint64_t k_mnmaj = smem_desc_sw128(smem_u32(smem + kOffK), kBlock, 1024);
+        const uint64_t ps_kmaj = smem_desc_sw128(smem_u32(smem + kOffPS), 16, 1024);
+        const uint64_t ps_mnmaj = smem_desc_sw128(smem_u32(smem + kOffPS), kBlock, 1024);
+        const uint32_t aQ0 = smem_u32(smem + kOffQ), aDO0 = smem_u32(smem + kOffDO);
+        // S^T or dP^T: K = 64 head-dim elements, one column block
+        auto issue_scores = [&](uint32_t d_col, uint64_t a_desc, uint32_t b_base) {
+          const uint64_t bd = smem_desc_sw128(b_base, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_ss(tmem + d_col, a_desc + kstep_kmajor(kk), bd + kstep_kmajor(kk), kIdS, kk > 0 ? 1u : 0u);
+        };
+        bool ok = wait_bar(&bars->kv_full, 0, abort_flag, p.status) &&
+                  wait_bar(&bars->qd_full[0], 0, abort_flag, p.status);
+        if (ok) {
+          tc_fence_after();
+          if (chain_x) {
+            issue_scores(kColX, k_kmaj, aQ0);
+            mma_commit(&bars->s_full);
+          } else {
+            issue_scores(kColY, v_kmaj, aDO0);
+            mma_commit(&bars->dp_full);
+          }
+        }
+        if (chain_x) {
+          for (int t = 0; ok && t < T; ++t) {
+            const int s = t % kStages;
+            const uint32_t ph = t & 1;
+            // dV += P^T dO_t: A = P^T in tensor memory, B = dO_t MN-major (N = 64)
+            if (!(ok = wait_bar(&bars->p_full, ph, abort_flag, p.status))) break;
+            tc_fence_after();
+            {
+              const uint64_t bd = smem_desc_sw128(aDO0 + s * kTile, kBlock, 1024);
+#pragma unroll
+              for (int kk = 0; kk < kT / 16; ++kk)
+                mma_f16_ts(tmem + kColDV, tmem + kColX + (kk / 4) * 64 + (kk % 4) * 8, bd + kstep_mnmajor(kk), kIdAcc,
+                           (t > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->dv_done);
+            mma_commit(&bars->qd_empty[s]);
+            if (t + 1 < T) {
+              const int s1 = (t + 1) % kStages;
+              if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / kStages) & 1, abort_flag, p.status))) break;
+              if (!(ok = wait_bar(&bars->dv_done, ph, abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_scores(kColX, k_kmaj, aQ0 + s1 * kTile);
+              mma_commit(&bars->s_full);
+            }
+          }
+        } else {
+          for (int t = 0; ok && t < T; ++t) {
+            const int s = t % kStages;
+            const uint32_t ph = t & 1;
+            if (t + 1 < T) {
+              const int s1 = (t + 1) % kStages;
+              if (!(ok = wait_bar(&bars->qd_full[s1], ((t + 1) / kStages) & 1, abort_flag, p.status))) break;
+              if (!(ok = wait_bar(&bars->dp_free, ph, abort_flag, p.status))) break;
+              tc_fence_after();
+              issue_scores(kColY, v_kmaj, aDO0 + s1 * kTile);
+              mma_commit(&bars->dp_full);
+            }
+            if (!(ok = wait_bar(&bars->ds_full, ph, abort_flag, p.status))) break;
+            if (t > 0 && !(ok = wait_bar(&bars->dq_free, (t - 1) & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            // dQ(t) = dS K: A = dS^T read MN-major (M = 128 queries), B = K MN-major (N = 64)
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_f16_ss(tmem + kColQ, ps_mnmaj + kstep_mnmajor(kk), k_mnmaj + kstep_mnmajor(kk), kIdDQ,
+                         kk > 0 ? 1u : 0u);
+            mma_commit(&bars->dq_full);
+            // dK += dS^T Q_t: the last reader of dS^T(t) and of Q_t
+            {
+              const uint64_t bd = smem_desc_sw128(aQ0 + s * kTile, kBlock, 1024);
+#pragma unroll
+              for (int kk = 0; kk < kT / 16; ++kk)
+                mma_f16_ss(tmem + kColDK, ps_kmaj + kstep_kmajor(kk), bd + kstep_mnmajor(kk), kIdAcc,
+                           (t > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&bars->dk_done);
+            mma_commit(&bars->qd_empty[s]);
+          }
+        }
+        mma_commit(&bars->acc_done);
+        int dummy = 0;
+        bounded_wait(&bars->acc_done, 0, reinterpret_cast<volatile int*>(&dummy), p.status, kStatusTimeoutDrain);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ================================================================ compute warpgroups
+    regs_inc<kRegsCompute>();
+    const int wg = warp / 4;
+    const int kl = (warp % 4) * 32 + lane;  // key row (TMEM lane of S^T / dP^T)
+    const int key = k0 + kl;
+    const uint32_t lane_off = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t colX = tmem + lane_off + kColX + wg * 64;
+    const uint32_t colY = tmem + lane_off + kColY + wg * 64;
+    const float lam = p.scale_log2;
+    float x[64];
+
+    auto phase_p = [&](int t) -> bool {
+      const int s = t % kStages;
+      int h, q0;
+      block_coords(t, h, q0);
+      (void)h;
+      const int c0 = q0 + wg * 64;
+      const bool ok = wait_bar(&bars->s_full, t & 1, abort_flag, p.status) &&
+                      wait_bar(&bars->qd_full[s], (t / kStages) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      tc_fence_after();
+      tmem_ld32(colX, *reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      tmem_ld32(colX + 32, *reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      tmem_wait_ld();
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[0]));
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&x[32]));
+      const float4* st_l = reinterpret_cast<const float4*>(stats + s * 2 * kT + wg * 64);
+      const bool need_mask = (k0 + kT > p.Sk) || (CAUSAL && (k0 + kT - 1 > c0 + p.delta));
+      const int first_c = (key >= p.Sk) ? 64 : (CAUSAL ? key - p.delta - c0 : 0);
+#pragma unroll
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 l4 = st_l[c4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = 4 * c4 + 2 * i;
+          const float2 e = ex2_pair(make_float2(fmaf(x[c], lam, -(i ? l4.z : l4.x)),
+                                                fmaf(x[c + 1], lam, -(i ? l4.w : l4.y))),
+                                    c / 2);
+          x[c] = (need_mask && c < first_c) ? 0.f : e.x;
+          x[c + 1] = (need_mask && c + 1 < first_c) ? 0.f : e.y;
+        }
+      }
+      {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(x[2 * i], x[2 * i + 1]);
+        tmem_st16(colX, pk);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(x[32 + 2 * i], x[32 + 2 * i + 1]);
+        tmem_st16(colX + 16, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bars->p_full);
+      return true;
+    };
+
+    auto phase_ds = [&](int t) -> bool {
+      const int s = t % kStages;
+      bool ok = wait_bar(&bars->dp_full, t & 1, abort_flag, p.status);
+      if (t > 0) ok = ok && wait_bar(&bars->dk_done, (t - 1) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      tc_fence_after();
+      const float4* st_d = reinterpret_cast<const float4*>(stats + s * 2 * kT + kT + wg * 64);
+      uint8_t* row = smem + kOffPS + wg * kBlock + kl * 128;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t w[32];
+        tmem_ld32(colY + hf * 32, w);
+        tmem_wait_ld();
+        reg_fence32(w);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = st_d[hf * 8 + c4];
+          const int cb = hf * 32 + 4 * c4;
+          pk[2 * c4] = pack2<BF16>(x[cb] * (__uint_as_float(w[4 * c4]) - d4.x),
+                                   x[cb + 1] * (__uint_as_float(w[4 * c4 + 1]) - d4.y));
+          pk[2 * c4 + 1] = pack2<BF16>(x[cb + 2] * (__uint_as_float(w[4 * c4 + 2]) - d4.z),
+                                       x[cb + 3] * (__uint_as_float(w[4 * c4 + 3]) - d4.w));
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int chunk = hf * 4 + c;
+          *reinterpret_cast<uint4*>(row + ((chunk ^ (kl & 7)) << 4)) =
+              make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->dp_free);  // dP^T(t) is in registers: dP^T(t+1) may follow
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->ds_full);
+      return true;
+    };
+
+    bool ok = T > 0 && phase_p(0);
+    for (int t = 0; ok && t < T; ++t) {
+      if (!(ok = phase_ds(t))) break;
+      if (t + 1 < T && !(ok = phase_p(t + 1))) break;
+    }
+
+    // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (x tau)
+    bool have = ok && T > 0;
+    if (have) {
+      have = wait_bar(&bars->acc_done, 0, abort_flag, p.status);
+      have = __all_sync(0xffffffffu, have);
+      tc_fence_after();
+    }
+    const float mul = wg ? p.scale : 1.f;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(wg ? p.dk : p.dv) + (static_cast<long long>(bkv) * p.Sk + key) * kD;
+#pragma unroll 1
+    for (int c = 0; c < kD / 32; ++c) {
+      uint32_t w[32];
+      if (have) {
+        tmem_ld32(tmem + lane_off + (wg ? kColDK : kColDV) + c * 32, w);
+        tmem_wait_ld();
+        reg_fence32(w);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = 0u;
+      }
+      if (key < p.Sk) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarpX) tmem_dealloc(tmem, 512);
+}
+
 // D[row] = sum_t dO[row,t] * O[row,t] (fp32) and a zeroed accumulator row;
-// 16 threads per row, 8 elements (16 bytes) each.
-template <bool BF16>
+// DH / 8 threads per row, 8 elements (16 bytes) each.
+template <int DH, bool BF16>
 __global__ void __launch_bounds__(256) bwd_atomic_prep_kernel(const uint16_t* __restrict__ o,
                                                               const uint16_t* __restrict__ dout,
                                                               float* __restrict__ Dvec, float* __restrict__ dq_acc,
                                                               long long n_rows) {
-  constexpr int kTpr = kD / 8;  // threads per row
+  constexpr int kTpr = DH / 8;  // threads per row
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long r = tid / kTpr;
   const int part = static_cast<int>(tid % kTpr);
   float acc = 0.f;
   if (r < n_rows) {
-    const uint4 a = *reinterpret_cast<const uint4*>(o + r * kD + part * 8);
-    const uint4 c = *reinterpret_cast<const uint4*>(dout + r * kD + part * 8);
+    const uint4 a = *reinterpret_cast<const uint4*>(o + r * DH + part * 8);
+    const uint4 c = *reinterpret_cast<const uint4*>(dout + r * DH + part * 8);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -576,7 +1041,7 @@ __global__ void __launch_bounds__(256) bwd_atomic_prep_kernel(const uint16_t* __
       acc = fmaf(a0, c0, acc);
       acc = fmaf(a1, c1, acc);
     }
-    float4* z = reinterpret_cast<float4*>(dq_acc + r * kD + part * 8);
+    float4* z = reinterpret_cast<float4*>(dq_acc + r * DH + part * 8);
     z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -606,26 +1071,32 @@ int head_group_atomic(long long per_head_bytes, long long heads) {
   return static_cast<int>(hg < heads ? hg : heads);
 }
 
-template <bool BF16, bool CAUSAL>
+template <int DH, bool BF16, bool CAUSAL>
 int launch_atomic_t(const BackwardArgs& a) {
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_tmap_3d(&tq, a.q, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
-      !make_tmap_3d(&tdo, a.dout, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
-      !make_tmap_3d(&tk, a.k, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
-      !make_tmap_3d(&tv, a.v, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if (!make_tmap_3d(&tq, a.q, BF16, DH, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tdo, a.dout, BF16, DH, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tk, a.k, BF16, DH, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
+      !make_tmap_3d(&tv, a.v, BF16, DH, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
+    return -1;
+  if (DH == 64 && !make_tmap_3d_f32(&tdq, a.dq_acc, DH, a.Sq, static_cast<long long>(a.B) * a.H, 32, 32))
     return -1;
   const long long n_rows = static_cast<long long>(a.B) * a.H * a.Sq;
   {
-    const long long blocks = (n_rows * (kD / 8) + 255) / 256;
+    const long long blocks = (n_rows * (DH / 8) + 255) / 256;
     if (blocks > 0x7FFFFFFFLL) return -1;
-    bwd_atomic_prep_kernel<BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
+    bwd_atomic_prep_kernel<DH, BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.Dvec, a.dq_acc, n_rows);
   }
+  const int smem_bytes = DH == 64 ? d64::kSmemBytes : kSmemBytes;
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
-    if (cudaFuncSetAttribute(bwd_atomic_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess)
-      return -1;
+    const cudaError_t e =
+        DH == 64 ? cudaFuncSetAttribute(bwd_atomic64_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes)
+                 : cudaFuncSetAttribute(bwd_atomic_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem_bytes);
+    if (e != cudaSuccess) return -1;
     attr_set = true;
   }
   AtomicParams p;
@@ -646,12 +1117,16 @@ int launch_atomic_t(const BackwardArgs& a) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.status = a.status;
-  p.head_group = head_group_atomic(static_cast<long long>(p.g) * a.Sq * kD * 8, static_cast<long long>(a.B) * a.Hkv);
+  p.head_group = head_group_atomic(static_cast<long long>(p.g) * a.Sq * DH * 8, static_cast<long long>(a.B) * a.Hkv);
   const long long grid = static_cast<long long>(a.B) * a.Hkv * p.n_ktiles;
   if (grid > 0x7FFFFFFFLL) return -1;
-  bwd_atomic_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, tdo, p);
+  if constexpr (DH == 64)
+    bwd_atomic64_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid), kThreads, smem_bytes, a.stream>>>(tq, tk, tv, tdo,
+                                                                                                      tdq, p);
+  else
+    bwd_atomic_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid), kThreads, smem_bytes, a.stream>>>(tq, tk, tv, tdo, p);
   {
-    const long long n8 = n_rows * (kD / 8);
+    const long long n8 = n_rows * (DH / 8);
     const long long blocks = (n8 + 255) / 256;
     if (blocks > 0x7FFFFFFFLL) return -1;
     bwd_dq_convert_kernel<BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
@@ -663,9 +1138,14 @@ int launch_atomic_t(const BackwardArgs& a) {
 }  // namespace
 
 int launch_backward_atomic(const BackwardArgs& a) {
-  if (a.d != kD || !a.dq_acc) return -1;
-  if (a.bf16) return a.causal ? launch_atomic_t<true, true>(a) : launch_atomic_t<true, false>(a);
-  return a.causal ? launch_atomic_t<false, true>(a) : launch_atomic_t<false, false>(a);
+  if (!a.dq_acc) return -1;
+  if (a.d == 128) {
+    if (a.bf16) return a.causal ? launch_atomic_t<128, true, true>(a) : launch_atomic_t<128, true, false>(a);
+    return a.causal ? launch_atomic_t<128, false, true>(a) : launch_atomic_t<128, false, false>(a);
+  }
+  if (a.d != 64) return -1;
+  if (a.bf16) return a.causal ? launch_atomic_t<64, true, true>(a) : launch_atomic_t<64, true, false>(a);
+  return a.causal ? launch_atomic_t<64, false, true>(a) : launch_atomic_t<64, false, false>(a);
 }
 
 }  // namespace gbattn

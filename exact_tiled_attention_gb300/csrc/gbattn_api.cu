@@ -94,6 +94,22 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, int d, int rows
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d_f32(CUtensorMap* map, void* base, int inner, int rows, long long outer, int box_inner,
+                      int box_rows) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (enc == nullptr || box_inner * 4 > 128) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner) * 4,
+                                 static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(inner) * 4};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Both exp2 paths of the kernels on n values: y_poly = ex2_poly3_x2 (FMA
 // pipe), y_hw = ex2.approx (MUFU).  n is even.
 __global__ void ex2_paths_kernel(const float* __restrict__ x, float* __restrict__ y_poly,
@@ -302,7 +318,7 @@ int attn_bwd_atomic(const void* q, const void* k, const void* v, const void* o, 
                     void* stream) {
   if (B < 1 || H < 1 || Hkv < 1 || Sq < 1 || Sk < 1) return GBATTN_EBADSHAPE;
   if (H % Hkv != 0) return GBATTN_EHEADS;
-  if (d != 128) return GBATTN_EHEADDIM;
+  if (d != 64 && d != 128) return GBATTN_EHEADDIM;
   if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
   const void* ptrs[] = {q, k, v, o, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)

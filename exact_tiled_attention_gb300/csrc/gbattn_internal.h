@@ -106,6 +106,12 @@ EncodeTiledFn encode_tiled_fn();
 bool make_tmap_3d(CUtensorMap* map, const void* base, bool bf16, int d, int rows, long long outer,
                   int box_rows);
 
+// 3-D tensor map over a contiguous [outer, rows, inner] fp32 tensor with a
+// (box_inner x box_rows x 1) box, box_inner * 4 <= 128 bytes, and 128-byte
+// swizzle; rows past `rows` are not read or written.
+bool make_tmap_3d_f32(CUtensorMap* map, void* base, int inner, int rows, long long outer, int box_inner,
+                      int box_rows);
+
 // 3-D tensor map over a contiguous [outer, rows, inner] byte tensor with a
 // (128 x box_rows x 1) box and 128-byte swizzle; rows past `rows` and bytes
 // past `inner` read as 0.  inner must be a multiple of 16.

@@ -123,6 +123,17 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 
+// 3-D tiled reduce-add of one box from shared memory into global memory
+// (elementwise fp32 add for an fp32 map); rows past the map's extent are
+// skipped.  Coordinates must not be negative; x * element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* smem_src, int x, int y, int z) {
+  asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // L2 eviction-priority policies (createpolicy).
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;

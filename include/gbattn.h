@@ -256,7 +256,7 @@ size_t attn_bwd_atomic_workspace_bytes(int B, int H, int Sq, int d);
  * adds every query block's contribution dS_ij K_j into the fp32 dQ
  * accumulator with atomic adds; a last kernel writes dQ = scale * accumulator
  * in the input dtype.  Same arguments, layouts and definition as attn_bwd
- * (d must be 128); workspace is caller-owned device scratch of at least
+ * (d = 64 or 128); workspace is caller-owned device scratch of at least
  * attn_bwd_atomic_workspace_bytes(B, H, Sq, d) bytes, 16-byte aligned, its
  * contents on entry irrelevant (the call zeroes the accumulator).
  *
@@ -265,7 +265,7 @@ size_t attn_bwd_atomic_workspace_bytes(int B, int H, int Sq, int d);
  * repeatable.  Five 128 x 128 products per (query block, key tile) pair
  * against attn_bwd's seven.
  *
- * Errors: as attn_bwd; GBATTN_EHEADDIM for d != 128.
+ * Errors: as attn_bwd.
  */
 int attn_bwd_atomic(const void *q, const void *k, const void *v, const void *o, const float *lse,
                     const void *dout, void *dq, void *dk, void *dv,

@@ -211,8 +211,8 @@ def test_bwd_atomic_validation(lib):
     assert _bwd_atomic(lib, B=0) == -1
     assert _bwd_atomic(lib, Sk=0) == -1
     assert _bwd_atomic(lib, H=6, Hkv=4) == -2
-    assert _bwd_atomic(lib, d=64) == -3
     assert _bwd_atomic(lib, d=96) == -3
+    assert _bwd_atomic(lib, d=32) == -3
     assert _bwd_atomic(lib, dtype=2) == -4
     for name in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv", "ws"):
         assert _bwd_atomic(lib, **{name: None}) == -5, name

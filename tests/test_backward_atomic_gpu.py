@@ -1,6 +1,8 @@
 """GPU parity of the atomic-dQ backward (C ABI attn_bwd_atomic) against the
 fp64 oracle, plus its contract: dK and dV repeat bitwise, dQ agrees with the
-two-owner backward to rounding, d = 64 and short workspaces are refused."""
+two-owner backward to rounding, other head dimensions and short workspaces
+are refused.  Head dimension 128 adds dQ with fp32 reductions from
+registers, 64 with TMA bulk tensor reductions: both are covered."""
 import math
 
 import pytest
@@ -30,6 +32,15 @@ def _dout(shape, dtype, seed):
 
 
 @pytest.mark.parametrize("shape", [
+    # head dim 64: the tiny fp16 workload, ragged tails, causal, GQA, Sq != Sk
+    (1, 4, 4, 128, 128, "fp16", False, 64),
+    (1, 2, 2, 300, 300, "fp16", True, 64),
+    (2, 4, 2, 257, 257, "bf16", True, 64),
+    (1, 2, 1, 200, 77, "fp16", True, 64),
+    (1, 2, 2, 129, 700, "bf16", False, 64),
+    (1, 2, 2, 64, 1000, "fp16", True, 64),
+    (1, 1, 1, 1, 1, "fp16", False, 64),
+    (1, 2, 2, 1024, 1024, "bf16", False, 64),
     (1, 1, 1, 128, 128, "bf16", False),
     (1, 2, 2, 300, 300, "bf16", True),     # ragged tails, diagonal blocks
     (1, 2, 2, 300, 300, "fp16", False),
@@ -44,8 +55,8 @@ def _dout(shape, dtype, seed):
     (1, 2, 2, 1024, 1024, "bf16", False),  # several query blocks per key tile
 ])
 def test_bwd_atomic_small_all_elements(shape):
-    B, H, Hkv, Sq, Sk, dt, causal = shape
-    d = 128
+    B, H, Hkv, Sq, Sk, dt, causal = shape[:7]
+    d = shape[7] if len(shape) > 7 else 128
     q, k, v = make_prefill(B, H, Hkv, Sq, Sk, d, DT[dt], 31, device="cuda")
     do = _dout((B, H, Sq, d), DT[dt], 32)
     scale = 1.0 / math.sqrt(d)
@@ -68,6 +79,8 @@ def test_bwd_atomic_scales(scale):
 
 
 @pytest.mark.parametrize("name,kv_ids", [
+    ("tiny_fwd_fp16", [0, 3]),
+    ("prefill_fp16_b1_h8_s4096_d64", [0, 7]),
     ("causal_bf16_b4_h16_s8192_d128", [0, 63]),
     ("gqa_causal_bf16_b2_hq32_hkv8_s4096_d128", [1, 14]),
 ])
@@ -118,8 +131,9 @@ def test_bwd_atomic_key_gradient_sums_to_zero():
 
 
 def test_bwd_atomic_refusals():
-    q, k, v = make_prefill(1, 2, 2, 100, 100, 64, torch.bfloat16, 61, device="cuda")
-    o, lse = attn_fwd(q, k, v)
+    q, k, v = make_prefill(1, 2, 2, 100, 100, 96, torch.bfloat16, 61, device="cuda")
+    o = torch.zeros_like(q)
+    lse = torch.zeros(1, 2, 100, dtype=torch.float32, device="cuda")
     with pytest.raises(GbattnError, match="EHEADDIM"):
         attn_bwd_atomic(q, k, v, o, lse, q)
     q, k, v = make_prefill(1, 2, 2, 100, 100, 128, torch.bfloat16, 62, device="cuda")
