@@ -41,6 +41,7 @@ def _dout(shape, dtype, seed):
     (1, 2, 2, 64, 1000, "fp16", True, 64),
     (1, 1, 1, 1, 1, "fp16", False, 64),
     (1, 2, 2, 1024, 1024, "bf16", False, 64),
+    (1, 8, 1, 300, 300, "fp16", True, 64),   # g = 8
     (1, 1, 1, 128, 128, "bf16", False),
     (1, 2, 2, 300, 300, "bf16", True),     # ragged tails, diagonal blocks
     (1, 2, 2, 300, 300, "fp16", False),
@@ -53,6 +54,7 @@ def _dout(shape, dtype, seed):
     (2, 2, 2, 1, 333, "fp16", True),
     (1, 2, 2, 333, 1, "bf16", False),
     (1, 2, 2, 1024, 1024, "bf16", False),  # several query blocks per key tile
+    (1, 8, 1, 300, 300, "bf16", True),     # g = 8
 ])
 def test_bwd_atomic_small_all_elements(shape):
     B, H, Hkv, Sq, Sk, dt, causal = shape[:7]

@@ -44,9 +44,10 @@ def test_forward_65536_sampled_rows(pair):
     assert_attn_close(o_got, lse_got, o_ref, lse_ref, f"S={S} {'pair' if pair else 'causal'}")
 
 
-def test_backward_32768_properties_and_paths_agree():
-    B, H, Hkv, Sq, d = 1, 2, 1, 32768, 128
-    q, k, v = make_prefill(B, H, Hkv, Sq, Sq, d, torch.bfloat16, 72, device="cuda")
+@pytest.mark.parametrize("d,dt", [(128, torch.bfloat16), (64, torch.float16)])
+def test_backward_32768_properties_and_paths_agree(d, dt):
+    B, H, Hkv, Sq = 1, 2, 1, 32768
+    q, k, v = make_prefill(B, H, Hkv, Sq, Sq, d, dt, 72, device="cuda")
     do = randn(q.shape, q.dtype, make_generator(73, "cuda"), "cuda")
     o, lse = attn_fwd(q, k, v, causal=True)
     a = attn_bwd(q, k, v, o, lse, do, causal=True)
