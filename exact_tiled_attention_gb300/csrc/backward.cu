@@ -973,15 +973,10 @@ int launch_bwd_t(const BackwardArgs& a) {
     bwd_preprocess_kernel<D, BF16><<<static_cast<unsigned>(blocks), 256, 0, a.stream>>>(
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.Dvec, n_rows);
   }
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(bwd_dkdv_kernel<D, BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             ColCfg<D>::kSmemBytes) != cudaSuccess ||
-        cudaFuncSetAttribute(bwd_dq_kernel<D, BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             RowCfg<D>::kSmemBytes) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> col_done{0}, row_done{0};  // per instantiation
+  if (!set_smem_limit_once(bwd_dkdv_kernel<D, BF16, CAUSAL>, ColCfg<D>::kSmemBytes, col_done) ||
+      !set_smem_limit_once(bwd_dq_kernel<D, BF16, CAUSAL>, RowCfg<D>::kSmemBytes, row_done))
+    return -1;
   BwdParams p;
   p.lse = a.lse;
   p.Dvec = a.Dvec;

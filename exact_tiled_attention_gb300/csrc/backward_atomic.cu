@@ -1089,16 +1089,10 @@ int launch_atomic_t(const BackwardArgs& a) {
         static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dout), a.Dvec, a.dq_acc, n_rows);
   }
   const int smem_bytes = DH == 64 ? d64::kSmemBytes : kSmemBytes;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    const cudaError_t e =
-        DH == 64 ? cudaFuncSetAttribute(bwd_atomic64_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        smem_bytes)
-                 : cudaFuncSetAttribute(bwd_atomic_kernel<BF16, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        smem_bytes);
-    if (e != cudaSuccess) return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per instantiation
+  const bool attr_ok = DH == 64 ? set_smem_limit_once(bwd_atomic64_kernel<BF16, CAUSAL>, smem_bytes, attr_done)
+                                : set_smem_limit_once(bwd_atomic_kernel<BF16, CAUSAL>, smem_bytes, attr_done);
+  if (!attr_ok) return -1;
   AtomicParams p;
   p.lse = a.lse;
   p.Dvec = a.Dvec;

@@ -406,13 +406,8 @@ int launch_decode_t(const DecodeArgs& a) {
       !make_tmap_3d(&tv, a.v, BF16, D, a.Sk_max, outer, kKeysPerSlot))
     return -1;
   auto kern = decode_partial_kernel<D, BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per instantiation
+  if (!set_smem_limit_once(kern, C::kSmemBytes, attr_done)) return -1;
   DecParams p;
   p.q = static_cast<const uint16_t*>(a.q);
   p.seqlens = a.seqlens;

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace gbattn {
 
 // Arguments of one prefill launch (already validated by the C-ABI layer).
@@ -100,6 +102,22 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device, once per device for each call site (`done` holds one bit per device
+// ordinal; devices past 63 set it on every call).  The attribute belongs to
+// the device's context, so a process that launches on several GPUs needs it
+// on each; concurrent host threads may both set it, which is harmless.
+template <typename Kernel>
+inline bool set_smem_limit_once(Kernel kernel, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  done.fetch_or(bit, std::memory_order_release);
+  return true;
+}
 
 // 3-D tensor map over a contiguous [outer, rows, d] 16-bit tensor with a
 // (64 x box_rows x 1) box and 128-byte swizzle; rows past `rows` read as 0.

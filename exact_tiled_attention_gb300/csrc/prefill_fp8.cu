@@ -500,12 +500,8 @@ int launch_fp8_t(const PrefillFp8Args& a) {
       !make_tmap_3d_u8(&tvt, a.vt, Sk_pad, kD, BHkv, kD))
     return -1;
   auto kern = prefill_fp8_kernel<CAUSAL>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per instantiation
+  if (!set_smem_limit_once(kern, kSmemBytes, attr_done)) return -1;
   Fp8Params p;
   p.o = a.o;
   p.lse = a.lse;

@@ -606,13 +606,8 @@ int launch_t(const PrefillArgs& a) {
       !make_tmap_3d(&tv, a.v, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN))
     return -1;
   auto kern = prefill_fwd_kernel<D, BF16, CAUSAL>;
-  static bool attr_set = false;  // per instantiation
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
-        cudaSuccess)
-      return -1;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};  // per instantiation
+  if (!set_smem_limit_once(kern, C::kSmemBytes, attr_done)) return -1;
   Params p;
   p.o = a.o;
   p.lse = a.lse;
