@@ -72,6 +72,33 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def host_info() -> dict:
+    """CPU model, host core count, torch and CUDA versions: recorded with every
+    CPU baseline (the oracle's rate depends on the host; the seeded inputs on
+    the torch version)."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith(("model name", "cpu part")):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"cpu_model": model or "unknown", "host_cores": os.cpu_count(), "torch": torch.__version__,
+            "cuda": torch.version.cuda,
+            "gpu": torch.cuda.get_device_name() if torch.cuda.is_available() else None}
+
+
 def prefill_flops(w) -> float:
     f = 4.0 * w.B * w.H * w.Sq * w.Sk * w.d
     return f / 2 if w.causal else f
@@ -395,7 +422,8 @@ def bench_prefill(args, world, rank, peaks, peak_kind, w=None, with_e2e=True, pa
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
                    "d": w.d, "causal": w.causal, "flops_per_step": flops,
                    "l2": l2_note,
-                   "parallelism": f"replicas x{world} (independent problems per GPU)"},
+                   "parallelism": f"replicas x{world} (independent problems per GPU)",
+                   "torch": torch.__version__},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} bf16 burst",
@@ -474,7 +502,8 @@ def bench_decode(args, world, rank, peaks, peak_kind, steps=None, warmup=None):
                    "n_split": w.n_split, "sum_valid_len": int(np.sum(lens)),
                    "algorithmic_bytes_per_step": nbytes,
                    "l2": "KV cache 8.6 GB > 129 MB L2; no flush",
-                   "parallelism": f"replicas x{world} (independent problems per GPU)"},
+                   "parallelism": f"replicas x{world} (independent problems per GPU)",
+                   "torch": torch.__version__},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_kind": f"{peak_kind} copy bandwidth"},
@@ -650,6 +679,42 @@ def cpu_oracle_decode(target_seconds: float):
         f"sequence {b} (valid length {int(lens[b])}), all {w.H} query heads, {reps} repeats, {dt:.1f} s")
 
 
+def cpu_oracle_backward(w):
+    """Time the fp64 backward oracle on one KV head of batch 0 of a backward
+    workload (all query heads of its group, every query row against its
+    visible keys).  Returns (TFLOP/s in the 2.5 x forward convention,
+    threads, sample description)."""
+    import oracle
+    from exact_tiled_attention_gb300.inputs import make_generator, randn
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    q, k, v = make_workload(w, device=dev)
+    do = randn(q.shape, q.dtype, make_generator(w.seed + 100, dev), dev)
+    g = w.H // w.Hkv
+    qs, dos = (t[0:1, 0:g].float().cpu().numpy() for t in (q, do))
+    ks, vs = (t[0:1, 0:1].float().cpu().numpy() for t in (k, v))
+    t0 = time.perf_counter()
+    oracle.attn_bwd_kvheads(qs, ks, vs, dos, w.scale, w.causal, [0])
+    dt = time.perf_counter() - t0
+    cells = float(w.Sq) * (w.Sk + 1) / 2 if w.causal else float(w.Sq) * w.Sk
+    flops = 10.0 * w.d * cells * g
+    return flops / dt / 1e12, oracle.num_threads(), (
+        f"{w.name}: KV head 0 of batch 0 ({g} query head(s), all {w.Sq} rows), {dt:.1f} s")
+
+
+def leg_roofline(leg: dict, kernel: str) -> dict:
+    """One compact row of the per-leg roofline table carried in the headline
+    line's roofline object."""
+    r = leg["roofline"]
+    row = {"workload": leg.get("workload") or leg.get("config", {}).get("workload"), "kernel": kernel,
+           "bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"], "unit": r["unit"],
+           "frac": r["frac"], "traffic": r["traffic"],
+           "ms": leg.get("ms_per_launch") or leg.get("ms_per_call") or leg.get("ms_per_step")}
+    if "cpu_baseline" in leg:
+        row["cpu_baseline"] = leg["cpu_baseline"]["value"]
+    return row
+
+
 def reference_arm(args, world):
     """The fp64 oracle as it stands, timed on the host cores: every step is a
     bounded sample of the workload (query rows of one head for prefill, one
@@ -711,7 +776,7 @@ def reference_arm(args, world):
             "data": "synthetic i.i.d. N(0,1), seeded",
             "config": {"workload": w.name, "sample_per_step": sample},
             "cpu_baseline": {"value": val, "unit": unit, "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **host_info()},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -814,15 +879,58 @@ def main():
             line["prefill"] = bench_prefill(args, world, rank, peaks, peak_kind)
     torch.cuda.synchronize()
     if rank == 0 and not args.no_cpu_baseline:
+        host = host_info()
+
+        def cpu_line(val, cores, sample, unit):
+            return {"value": val, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample, **host}
+
         if args.workload != "decode":
-            val, cores, sample = cpu_oracle_prefill(
-                args.cpu_seconds, None if args.workload == "prefill" else WORKLOADS[args.workload])
-            line["cpu_baseline"] = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                    "sample": sample}
+            line["cpu_baseline"] = cpu_line(*cpu_oracle_prefill(
+                args.cpu_seconds, None if args.workload == "prefill" else WORKLOADS[args.workload]), "TFLOP/s")
         else:
-            val, cores, sample = cpu_oracle_decode(args.cpu_seconds)
-            line["cpu_baseline"] = {"value": val, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                                    "sample": sample}
+            line["cpu_baseline"] = cpu_line(*cpu_oracle_decode(args.cpu_seconds), "GB/s")
+        # every other leg: the oracle on a bounded sample of that leg's workload
+        leg_seconds = max(1.0, args.cpu_seconds / 4)
+        if isinstance(line.get("decode"), dict):
+            line["decode"]["cpu_baseline"] = cpu_line(*cpu_oracle_decode(leg_seconds), "GB/s")
+        if isinstance(line.get("prefill"), dict):
+            line["prefill"]["cpu_baseline"] = cpu_line(*cpu_oracle_prefill(leg_seconds), "TFLOP/s")
+        by_workload = {}
+        for leg in line.get("prefill_other", []):
+            leg["cpu_baseline"] = cpu_line(*cpu_oracle_prefill(leg_seconds, WORKLOADS[leg["workload"]]),
+                                           "TFLOP/s")
+            by_workload[leg["workload"]] = leg["cpu_baseline"]
+        if isinstance(line.get("cta_pair"), dict) and line["cta_pair"]["workload"] in by_workload:
+            line["cta_pair"]["cpu_baseline"] = by_workload[line["cta_pair"]["workload"]]
+        if isinstance(line.get("fp8"), dict):
+            line["fp8"]["cpu_baseline"] = dict(line["cpu_baseline"], sample=line["cpu_baseline"]["sample"]
+                                               + " (the oracle takes the dequantized inputs at the same rate)")
+        bwd_cpu = {}
+        for legs in (line.get("backward", []), line.get("backward_atomic", [])):
+            for leg in legs:
+                if leg["workload"] not in bwd_cpu:
+                    bwd_cpu[leg["workload"]] = cpu_line(*cpu_oracle_backward(WORKLOADS[leg["workload"]]),
+                                                        "TFLOP/s")
+                leg["cpu_baseline"] = bwd_cpu[leg["workload"]]
+    if "roofline" in line:
+        # the per-leg roofline table, in the headline's roofline object
+        rows = []
+        if isinstance(line.get("decode"), dict):
+            rows.append(leg_roofline(line["decode"], "decode_partial_kernel + decode_merge_kernel"))
+        if isinstance(line.get("prefill"), dict):
+            rows.append(leg_roofline(line["prefill"], "prefill_fwd_kernel"))
+        for leg in line.get("prefill_other", []):
+            rows.append(leg_roofline(leg, "prefill_fwd_kernel"))
+        if isinstance(line.get("cta_pair"), dict):
+            rows.append(leg_roofline(line["cta_pair"], "prefill_pair_kernel"))
+        if isinstance(line.get("fp8"), dict):
+            rows.append(leg_roofline(line["fp8"], "v_transpose_kernel + prefill_fp8_kernel"))
+        for leg in line.get("backward", []):
+            rows.append(leg_roofline(leg, "attn_bwd (3 kernels)"))
+        for leg in line.get("backward_atomic", []):
+            rows.append(leg_roofline(leg, "attn_bwd_atomic (3 kernels)"))
+        if rows:
+            line["roofline"]["legs"] = rows
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -196,6 +196,48 @@ def attn_decode_workspace_bytes(B: int, Hq: int, n_split: int, d: int) -> int:
     return int(load_library().attn_decode_workspace_bytes(B, Hq, n_split, d))
 
 
+def _check_decode(q, k_cache, v_cache, seqlens, out, lse):
+    """Metadata checks shared by both decode wrappers: tensor types and ranks,
+    then every shape and dtype agreement, then device and layout.  Returns
+    (B, Hq, Hkv, Sk_max, d)."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{n} must be a torch.Tensor")
+        if t.dim() != 4:
+            raise ValueError(f"{n} must have 4 dims, got shape {tuple(t.shape)}")
+    if not isinstance(seqlens, torch.Tensor):
+        raise TypeError("seqlens must be a torch.Tensor")
+    B, Hq, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes exactly one query per sequence: q [B,Hq,1,d]")
+    Bk, Hkv, Sk_max, dk = k_cache.shape
+    if k_cache.shape != v_cache.shape:
+        raise ValueError(f"k_cache {tuple(k_cache.shape)} and v_cache {tuple(v_cache.shape)} differ")
+    if Bk != B or dk != d:
+        raise ValueError(f"cache batch/head dim {Bk}/{dk} do not match q's {B}/{d}")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q and the caches must share one dtype")
+    _dtype_code(q)
+    if seqlens.dtype != torch.int32:
+        raise TypeError(f"seqlens must be int32, got {seqlens.dtype}")
+    if seqlens.dim() != 1 or seqlens.numel() != B:
+        raise ValueError(f"seqlens must hold one length per sequence ({B}), got shape {tuple(seqlens.shape)}")
+    if out is not None and (not isinstance(out, torch.Tensor) or out.shape != q.shape or out.dtype != q.dtype):
+        raise ValueError("out must be a tensor of q's shape and dtype")
+    if lse is not None and (not isinstance(lse, torch.Tensor) or tuple(lse.shape) != (B, Hq)
+                            or lse.dtype != torch.float32):
+        raise ValueError(f"lse must be a float32 tensor [{B}, {Hq}]")
+    _check(q, "q", 4)
+    _check(k_cache, "k_cache", 4)
+    _check(v_cache, "v_cache", 4)
+    if not seqlens.is_cuda or not seqlens.is_contiguous():
+        raise ValueError("seqlens must be a contiguous CUDA tensor")
+    for t, n in ((out, "out"), (lse, "lse")):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous CUDA tensor")
+    return B, Hq, Hkv, Sk_max, d
+
+
 def attn_decode_splitkv(q, k_cache, v_cache, seqlens, scale: float | None = None, n_split: int = 16,
                         workspace=None, out=None, lse=None, return_lse: bool = True, stream=None):
     """One-query split-KV decode through the C ABI `attn_decode_splitkv`.
@@ -204,19 +246,7 @@ def attn_decode_splitkv(q, k_cache, v_cache, seqlens, scale: float | None = None
     workspace: optional caller-owned fp32/uint8 CUDA buffer of at least
     attn_decode_workspace_bytes(B, Hq, n_split, d) bytes (allocated here if
     omitted).  Returns (o [B,Hq,1,d], lse [B,Hq] or None, workspace)."""
-    _check(q, "q", 4)
-    _check(k_cache, "k_cache", 4)
-    _check(v_cache, "v_cache", 4)
-    if not isinstance(seqlens, torch.Tensor) or not seqlens.is_cuda or seqlens.dtype != torch.int32:
-        raise ValueError("seqlens must be an int32 CUDA tensor")
-    B, Hq, one, d = q.shape
-    if one != 1:
-        raise ValueError("decode takes exactly one query per sequence: q [B,Hq,1,d]")
-    Bk, Hkv, Sk_max, dk = k_cache.shape
-    if k_cache.shape != v_cache.shape or Bk != B or dk != d or seqlens.numel() != B:
-        raise ValueError("shape mismatch between q, caches and seqlens")
-    if not (q.dtype == k_cache.dtype == v_cache.dtype):
-        raise TypeError("q and the caches must share one dtype")
+    B, Hq, Hkv, Sk_max, d = _check_decode(q, k_cache, v_cache, seqlens, out, lse)
     dt = _dtype_code(q)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -246,11 +276,7 @@ def attn_decode_splitkv_noalloc(q, k_cache, v_cache, seqlens, scale: float | Non
     cannot allocate device memory: the partial states go to the library's
     fixed 32 MiB device array (shared by all calls; order overlapping calls).
     Outputs are allocated here only when `out`/`lse` are not given."""
-    _check(q, "q", 4)
-    _check(k_cache, "k_cache", 4)
-    _check(v_cache, "v_cache", 4)
-    B, Hq, _, d = q.shape
-    Hkv, Sk_max = k_cache.shape[1], k_cache.shape[2]
+    B, Hq, Hkv, Sk_max, d = _check_decode(q, k_cache, v_cache, seqlens, out, lse)
     dt = _dtype_code(q)
     if scale is None:
         scale = 1.0 / math.sqrt(d)

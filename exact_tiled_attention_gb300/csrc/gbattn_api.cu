@@ -21,9 +21,10 @@ namespace {
 std::once_flag g_encode_once;
 EncodeTiledFn g_encode = nullptr;
 
-// Device status pointer per device (looked up once, then cached).
+// Device status pointer per device (looked up once per context, then cached).
 constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices] = {};
+unsigned long long g_status_ctx[kMaxDevices] = {};
 int g_sm_major[kMaxDevices] = {};
 int g_sm_minor[kMaxDevices] = {};
 std::mutex g_dev_mutex;
@@ -37,8 +38,9 @@ int current_device(int** status) {
     cudaGetLastError();
     return GBATTN_EUNSUPPORTED;
   }
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_dev_mutex);
-  if (g_status_ptr[dev] == nullptr) {
+  if (g_status_ptr[dev] == nullptr || ctx != g_status_ctx[dev]) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
@@ -54,6 +56,7 @@ int current_device(int** status) {
       return GBATTN_ELAUNCH;
     }
     g_status_ptr[dev] = static_cast<int*>(ptr);
+    g_status_ctx[dev] = current_context_id();  // the lookup made the primary context current
   }
   if (g_sm_major[dev] != 10 || g_sm_minor[dev] != 3) return GBATTN_EUNSUPPORTED;
   *status = g_status_ptr[dev];
@@ -61,6 +64,47 @@ int current_device(int** status) {
 }
 
 }  // namespace
+
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(fn);
+    cudaGetLastError();
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+int check_decode_args(const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+                      const void* o, const float* lse, int B, int Hq, int Hkv, int Sk_max, int d,
+                      int n_split, int dtype) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Sk_max < 1) return GBATTN_EBADSHAPE;
+  if (B > 65535) return GBATTN_EBADSHAPE;
+  if (Hq % Hkv != 0) return GBATTN_EHEADS;
+  if (d != 64 && d != 128) return GBATTN_EHEADDIM;
+  if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
+  if (n_split < 1 || n_split > 256) return GBATTN_ESPLIT;
+  if (!q || !k_cache || !v_cache || !seqlens || !o || !aligned16(q) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(o) || (reinterpret_cast<uintptr_t>(seqlens) & 3u) ||
+      (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return GBATTN_EPOINTER;
+  return GBATTN_OK;
+}
 
 EncodeTiledFn encode_tiled_fn() {
   std::call_once(g_encode_once, [] {
@@ -221,16 +265,10 @@ int attn_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
                         void* o, float* lse, int B, int Hq, int Hkv, int Sk_max, int d, float scale,
                         int n_split, void* workspace, size_t workspace_bytes, int dtype,
                         void* stream) {
-  if (B < 1 || Hq < 1 || Hkv < 1 || Sk_max < 1) return GBATTN_EBADSHAPE;
-  if (B > 65535) return GBATTN_EBADSHAPE;
-  if (Hq % Hkv != 0) return GBATTN_EHEADS;
-  if (d != 64 && d != 128) return GBATTN_EHEADDIM;
-  if (dtype != GBATTN_F16 && dtype != GBATTN_BF16) return GBATTN_EDTYPE;
-  if (n_split < 1 || n_split > 256) return GBATTN_ESPLIT;
-  if (!q || !k_cache || !v_cache || !seqlens || !o || !workspace || !aligned16(q) ||
-      !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(seqlens) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
-    return GBATTN_EPOINTER;
+  const int check = check_decode_args(q, k_cache, v_cache, seqlens, o, lse, B, Hq, Hkv, Sk_max, d,
+                                      n_split, dtype);
+  if (check != GBATTN_OK) return check;
+  if (!workspace || !aligned16(workspace)) return GBATTN_EPOINTER;
   if (workspace_bytes < attn_decode_workspace_bytes(B, Hq, n_split, d)) return GBATTN_EWORKSPACE;
   int* status = nullptr;
   int rc = current_device(&status);

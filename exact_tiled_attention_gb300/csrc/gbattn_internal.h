@@ -95,6 +95,19 @@ int launch_backward(const BackwardArgs& a);
 int launch_backward_atomic(const BackwardArgs& a);
 int launch_prefill_fp8(const PrefillFp8Args& a);
 
+// Checks the scalar and pointer arguments of a split-KV decode (everything
+// attn_decode_splitkv checks except the workspace); GBATTN_OK or the error.
+int check_decode_args(const void* q, const void* k_cache, const void* v_cache, const int* seqlens,
+                      const void* o, const float* lse, int B, int Hq, int Hkv, int Sk_max, int d,
+                      int n_split, int dtype);
+
+// Unique id of the CUDA context current on the calling thread (cuCtxGetId,
+// through the runtime's driver entry points), or 0 when no context is current
+// or the driver does not provide the calls.  A cached device address (a
+// __device__ symbol's) is valid only within the context it was looked up in:
+// after cudaDeviceReset the device's next primary context has a new id.
+unsigned long long current_context_id();
+
 // cuTensorMapEncodeTiled fetched once through the runtime's driver entry
 // point (no link-time dependency on libcuda).
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,

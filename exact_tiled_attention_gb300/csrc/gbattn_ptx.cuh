@@ -468,14 +468,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 // Software 2^x for two values on the FMA/ALU pipes instead of the MUFU unit
-// (M4.6 "FlashAttention-3/4 Hardware Pipelines" 0x09, software exp2):
-// range reduction 2^x = 2^n p(f) with n = floor(x), f = x - n in [0, 1), and
-// p the degree-3 polynomial with p(0) = 1 that minimises the maximum relative
-// error on [0, 1] (coefficients from exp2_poly_fit.py; 8.6e-5 in exact
-// arithmetic).  floor(x) comes from adding 1.5 * 2^23 with round-down, whose
-// low mantissa bits then hold n; 2^n is applied by adding n to the exponent
-// field of p(f).  Inputs are clamped to [-126, 127]: below -126 the result is
-// 2^-126 (a probability of ~1e-38 instead of 0).
+// (M4.6 "FlashAttention-3/4 Hardware Pipelines" 0x09 motivates offloading
+// part of the softmax exponentials this way).  The method is the textbook
+// one for exponentials: Cody-Waite style additive range reduction
+// 2^x = 2^n * 2^f with n = floor(x), f = x - n in [0, 1) (exact in fp32 for
+// base 2), a minimax polynomial for 2^f (degree 3, p(0) = 1, maximum
+// relative error 8.6e-5 on [0, 1], fitted here by the Remez exchange in
+// exp2_poly_fit.py), and reconstruction by adding n to the binary exponent
+// field (the ldexp step).  floor(x) is taken with the round-to-integer
+// constant 1.5 * 2^23 added under round-toward-minus-infinity, which leaves
+// n in the low mantissa bits of the sum.  Inputs are clamped to
+// [-126, 127]: below -126 the result is 2^-126 (a probability of ~1e-38
+// instead of 0).
 __device__ __forceinline__ float2 ex2_poly3_x2(float2 x) {
   constexpr float kC1 = 6.951167864e-01f, kC2 = 2.276449912e-01f, kC3 = 7.706704199e-02f;
   constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: spacing 1 around it

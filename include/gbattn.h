@@ -288,10 +288,22 @@ int attn_bwd_atomic(const void *q, const void *k, const void *v, const void *o, 
  * GBATTN_EWORKSPACE before any device work.  The call allocates nothing.
  *
  * The first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture.
- * Every call shares the array (nothing in it needs clearing: each call
- * overwrites the states it reads), so two calls whose kernels may overlap on
- * the GPU race and must be ordered by the caller.
+ * that device current.  CUDA loads device code lazily by default, so that
+ * first call is also the one that loads this part of the library onto the
+ * device, the 32 MiB array included, which may allocate and synchronise
+ * inside the CUDA runtime.  A caller that must never reach the allocator
+ * therefore makes one call (any valid problem) at initialisation, outside
+ * any stream capture; later calls allocate nothing.  The address is cached
+ * per device with the id of its CUDA context and looked up again if the
+ * context changes (after cudaDeviceReset), in which case that call is again
+ * a first call.  Every call shares the array (nothing in it needs clearing:
+ * each call overwrites the states it reads), so two calls whose kernels may
+ * overlap on the GPU race and must be ordered by the caller.
+ *
+ * Errors: the argument checks and codes of attn_decode_splitkv (EBADSHAPE,
+ * EHEADS, EHEADDIM, EDTYPE, EPOINTER, ESPLIT) come first; then
+ * GBATTN_EWORKSPACE for a problem too large for the array; EUNSUPPORTED,
+ * ELAUNCH.
  */
 int attn_decode_splitkv_noalloc(const void *q, const void *k_cache, const void *v_cache,
                                 const int *seqlens, void *o, float *lse,
@@ -345,11 +357,17 @@ int gbattn_exp2_paths(const float *x, float *y_poly, float *y_hw, long long n, v
 int gbattn_selftest_bounded_wait(int arrive, void *stream);
 
 /*
- * gbattn_device_status -- read and clear the library's device status word
- * (synchronises the current device).  Returns GBATTN_OK, or
- * GBATTN_EDEVICE_TIMEOUT if a kernel gave up since the last call (a bounded
- * wait timed out, or a shared-memory alignment check failed), or
- * GBATTN_ELAUNCH if the device reported an error.
+ * gbattn_device_status -- read and clear the library's device status word.
+ * Returns GBATTN_OK, or GBATTN_EDEVICE_TIMEOUT if a kernel gave up since the
+ * last call (a bounded wait timed out, or a shared-memory alignment check
+ * failed), or GBATTN_ELAUNCH if the device reported an error.
+ *
+ * Scope: the call synchronises the whole current device
+ * (cudaDeviceSynchronize, every stream), and the word is one per device,
+ * shared by all streams and host threads that use the library there.  A
+ * failure raised by a kernel on one stream is therefore reported to
+ * whichever caller polls first, and that call clears it; callers that share
+ * a device and need to attribute a failure must poll from one place.
  */
 int gbattn_device_status(void);
 

@@ -221,3 +221,72 @@ def test_bwd_atomic_validation(lib):
     need = lib.attn_bwd_atomic_workspace_bytes(1, 4, 8, 128)
     assert need == 256 + 4 * 8 * 128 * 4
     assert _bwd_atomic(lib, wsb=need - 1) == -6
+
+
+def _dec_noalloc(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, sl=FAKE, o=FAKE, lse=None, B=2, Hq=8, Hkv=2, Skm=64, d=128,
+             scale=0.1, n=4, dtype=1, stream=None)
+    a.update(kw)
+    return lib.attn_decode_splitkv_noalloc(a["q"], a["k"], a["v"], a["sl"], a["o"], a["lse"], a["B"],
+                                           a["Hq"], a["Hkv"], a["Skm"], a["d"], a["scale"], a["n"],
+                                           a["dtype"], a["stream"])
+
+
+def test_decode_noalloc_validation_precedes_capacity(lib):
+    """The no-allocation decode reports each bad argument with the code
+    attn_decode_splitkv gives it, even where the (bogus) problem would also
+    overflow the fixed scratch array; only a valid problem too large for the
+    array gets GBATTN_EWORKSPACE."""
+    cap = lib.attn_decode_noalloc_scratch_bytes()
+    assert cap == 32 << 20
+    assert _dec_noalloc(lib, n=0) == -9
+    assert _dec_noalloc(lib, n=300) == -9
+    assert _dec_noalloc(lib, n=300, B=4096, Hq=64, Hkv=8) == -9     # would need far more than 32 MiB
+    assert _dec_noalloc(lib, d=96) == -3
+    assert _dec_noalloc(lib, d=96, B=4096, Hq=64, Hkv=8) == -3
+    assert _dec_noalloc(lib, dtype=5) == -4
+    assert _dec_noalloc(lib, dtype=5, B=4096, Hq=64, Hkv=8) == -4
+    assert _dec_noalloc(lib, sl=None) == -5
+    assert _dec_noalloc(lib, sl=FAKE + 2) == -5
+    assert _dec_noalloc(lib, o=FAKE + 8) == -5
+    assert _dec_noalloc(lib, B=0) == -1
+    assert _dec_noalloc(lib, Hq=6, Hkv=4) == -2
+    # valid arguments, but the partial states need more than the array holds
+    B, Hq, n, d = 4096, 64, 16, 128
+    assert lib.attn_decode_workspace_bytes(B, Hq, n, d) > cap
+    assert _dec_noalloc(lib, B=B, Hq=Hq, Hkv=8, n=n, d=d) == -6
+
+
+@pytest.mark.parametrize("wrapper", ["attn_decode_splitkv", "attn_decode_splitkv_noalloc"])
+def test_decode_wrappers_reject_mismatched_tensors(wrapper):
+    """Both Python decode wrappers check every shape, dtype and length
+    agreement before any pointer reaches the library (a smaller v_cache or a
+    short seqlens would otherwise make the kernels read out of bounds)."""
+    fn = getattr(binding, wrapper)
+    B, Hq, Hkv, S, d = 2, 8, 2, 64, 128
+    bf = torch.bfloat16
+    q = torch.zeros(B, Hq, 1, d, dtype=bf)
+    k = torch.zeros(B, Hkv, S, d, dtype=bf)
+    sl = torch.full((B,), S, dtype=torch.int32)
+    cases = [
+        (ValueError, dict(q=torch.zeros(B, Hq, 2, d, dtype=bf))),                 # two queries per sequence
+        (ValueError, dict(v=torch.zeros(B, Hkv, S // 2, d, dtype=bf))),           # shorter v_cache
+        (ValueError, dict(k=torch.zeros(B + 1, Hkv, S, d, dtype=bf),
+                          v=torch.zeros(B + 1, Hkv, S, d, dtype=bf))),            # cache batch differs
+        (ValueError, dict(k=torch.zeros(B, Hkv, S, 64, dtype=bf),
+                          v=torch.zeros(B, Hkv, S, 64, dtype=bf))),               # head dim differs
+        (ValueError, dict(sl=torch.full((B - 1,), S, dtype=torch.int32))),         # short seqlens
+        (TypeError, dict(sl=torch.full((B,), S, dtype=torch.int64))),              # int64 lengths
+        (TypeError, dict(v=torch.zeros(B, Hkv, S, d, dtype=torch.float16))),       # dtypes differ
+        (TypeError, dict(q=torch.zeros(B, Hq, 1, d, dtype=torch.float32),
+                         k=torch.zeros(B, Hkv, S, d, dtype=torch.float32),
+                         v=torch.zeros(B, Hkv, S, d, dtype=torch.float32))),       # unsupported dtype
+        (ValueError, dict(out=torch.zeros(B, Hq, 1, 64, dtype=bf))),               # wrong out shape
+        (ValueError, dict(lse=torch.zeros(B, Hq + 1, dtype=torch.float32))),       # wrong lse shape
+        (ValueError, dict()),                                                      # consistent, but not CUDA
+    ]
+    for exc, over in cases:
+        a = dict(q=q, k=k, v=k.clone(), sl=sl, out=None, lse=None)
+        a.update(over)
+        with pytest.raises(exc):
+            fn(a["q"], a["k"], a["v"], a["sl"], out=a["out"], lse=a["lse"])

@@ -32,3 +32,23 @@ def test_traffic_record_needs_matching_workload_and_source(tmp_path, monkeypatch
     assert bench.ncu_traffic("other", sources, "causal_bf16_b4_h16_s8192_d128") is None
     src.write_bytes(src.read_bytes() + b"\n// changed\n")
     assert bench.ncu_traffic(key, sources, "causal_bf16_b4_h16_s8192_d128") is None  # stale source
+
+
+def test_host_info_names_cpu_and_versions():
+    h = bench.host_info()
+    assert h["cpu_model"] and h["cpu_model"] != ""
+    assert h["host_cores"] >= 1 and h["torch"] == bench.torch.__version__
+
+
+def test_cpu_oracle_backward_on_tiny_workload():
+    val, cores, sample = bench.cpu_oracle_backward(bench.WORKLOADS["tiny_fwd_fp16"])
+    assert val > 0 and cores >= 1 and "KV head 0" in sample
+
+
+def test_leg_roofline_row_keeps_the_figures():
+    leg = {"workload": "w", "ms_per_call": 1.5, "cpu_baseline": {"value": 0.01},
+           "roofline": {"bound": "tensor", "achieved": 10.0, "peak": 20.0, "unit": "TFLOP/s", "frac": 0.5,
+                        "traffic": None}}
+    row = bench.leg_roofline(leg, "k")
+    assert row == {"workload": "w", "kernel": "k", "bound": "tensor", "achieved": 10.0, "peak": 20.0,
+                   "unit": "TFLOP/s", "frac": 0.5, "traffic": None, "ms": 1.5, "cpu_baseline": 0.01}

@@ -106,7 +106,8 @@ def _sample_rows(w, n_random, seed):
 
 @pytest.mark.parametrize("name", ["tiny_fwd_fp16", "prefill_fp16_b1_h8_s4096_d64",
                                   "causal_bf16_b4_h16_s8192_d128",
-                                  "gqa_causal_bf16_b2_hq32_hkv8_s4096_d128"])
+                                  "gqa_causal_bf16_b2_hq32_hkv8_s4096_d128",
+                                  "noncausal_bf16_b4_h16_s8192_d128"])
 def test_workload_sampled_rows(name):
     w = WORKLOADS[name]
     q, k, v = make_prefill(w.B, w.H, w.Hkv, w.Sq, w.Sk, w.d, w.dtype, w.seed, device="cuda")

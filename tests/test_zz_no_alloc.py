@@ -75,3 +75,32 @@ def test_noalloc_rejects_problems_larger_than_its_array():
     rc = lib.attn_decode_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), sl.data_ptr(),
                                          q.data_ptr(), None, B, Hq, Hkv, 16, d, 0.1, n_split, 1, None)
     assert rc == -6
+
+
+def test_noalloc_at_the_64_sequence_workload_matches_the_oracle():
+    """The 64-sequence, 32768-slot decode workload (17 MB of partial states,
+    inside the fixed array) through the no-allocation entry point: every head
+    of sampled sequences, including the shortest and longest, against the fp64
+    oracle, and the whole result equal to the workspace entry point's."""
+    import oracle
+    from exact_tiled_attention_gb300.inputs import WORKLOADS, make_decode
+    from tests.parity_util import assert_attn_close, host_f32
+
+    w = WORKLOADS["decode_splitkv_bf16_b64_hq32_hkv8_sk32768_d128"]
+    lib = binding.load_library()
+    assert lib.attn_decode_workspace_bytes(w.B, w.H, w.n_split, w.d) <= lib.attn_decode_noalloc_scratch_bytes()
+    q, k, v, sl = make_decode(w.B, w.H, w.Hkv, w.Sk, w.d, w.dtype, w.len_lo, w.len_hi, w.seed, device="cuda")
+    rc, o, lse = _noalloc_call(lib, q, k, v, sl, w.n_split)
+    assert rc == 0, binding.error_string(rc)
+    torch.cuda.synchronize()
+    assert binding.gbattn_device_status() == 0
+    lens = sl.cpu().numpy()
+    rng = np.random.default_rng(11)
+    bs = sorted(set(rng.integers(0, w.B, size=6).tolist()) | {int(np.argmin(lens)), int(np.argmax(lens))})
+    for b in bs:
+        o_ref, lse_ref = oracle.attn_decode(host_f32(q[b:b + 1]), host_f32(k[b:b + 1]), host_f32(v[b:b + 1]),
+                                            lens[b:b + 1], w.scale)
+        assert_attn_close(o[b:b + 1], lse[b:b + 1], o_ref, lse_ref, f"no-alloc decode, batch {b}")
+    o_ws, lse_ws, _ = binding.attn_decode_splitkv(q, k, v, sl, scale=w.scale, n_split=w.n_split)
+    torch.cuda.synchronize()
+    _close(o, lse, o_ws, lse_ws)
