@@ -10,17 +10,26 @@
 // Tensor memory (512 columns, 128 lanes; lane = query row of the tile):
 //   S_H  [  0,128)  fp32 scores of tile H      S_L  [128,256)  of tile L
 //   O_H  [256,256+d)  unnormalised output      O_L  [256+d,256+2d)
+//   d = 64 only: P_H [384,448), P_L [448,512)  16-bit P, keys (2c, 2c+1) in column c
 // (the M4.6 0x07 capacity rule 2N + 2 d_v <= 512).
 //
-// Shared memory: Q_H, Q_L; P_H, P_L (16-bit probabilities, K-major with the
-// 128-byte swizzle, the A operand of the P.V MMA); a ring of K/V slots.
+// Shared memory: Q_H, Q_L; d = 128: P_H, P_L (16-bit probabilities, K-major
+// with the 128-byte swizzle, the A operand of the P.V MMA); a ring of K/V
+// slots.
 //
-// Why P lives in shared memory: with P aliased into its S columns (the
-// pages' FA4 map), QK(j+1) may only start after PV(j) has read P(j), so
-// every tile's softmax sits on the critical path of the tensor pipe.  With
-// P in its own buffer, QK_X(j+1) is issued as soon as the softmax threads
-// have copied S_X(j) into registers; each tile's softmax then runs back to
-// back and the tensor pipe, fed by both tiles, is the bound.
+// Why P does not alias S: with P written over its S columns (the pages'
+// FA4 map), QK(j+1) may only start after PV(j) has read P(j), so every
+// tile's softmax sits on the critical path of the tensor pipe.  With P in a
+// buffer of its own, QK_X(j+1) is issued as soon as the softmax threads have
+// copied S_X(j) into registers.  At d = 128 tensor memory is full (S and O
+// of both tiles), so P goes to shared memory and P.V reads both operands
+// from there (8 KB per 16-key step for 16 KB of tensor work: balanced).  At
+// d = 64 the P.V product has N = 64, so a shared-memory A operand would be
+// re-read for half the columns and the MMA would wait on shared-memory
+// bandwidth (measured: ~90 cycles per 16-key step, and the issuing thread
+// blocks behind it); the 128 columns S and O leave free hold P for both
+// tiles, and P.V reads A from tensor memory (a TS MMA) and only V from
+// shared memory.
 //
 // Warp roles (384 threads = three warpgroups):
 //   warps 0-3   softmax + correction + epilogue of tile H (thread = one row)
@@ -74,11 +83,15 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units (fp16/bf16 row of M4.6 
 
 template <int D>
 struct Cfg {
+  // d = 64: P lives in tensor memory (the 128 columns S and O leave free) and
+  // P.V reads it from there; d = 128: tensor memory is full, P is staged in
+  // shared memory.
+  static constexpr bool kPInTmem = (D == 64);
   static constexpr int kColBlocks = D / 64;           // 128-byte swizzle column blocks
   static constexpr int kTileBytes = kBM * D * 2;      // one 128 x D 16-bit tile
   static constexpr int kBlockBytes = kBM * 128;       // one 128-row x 128-byte block
-  static constexpr int kPBytes = kBM * kBN * 2;       // one 128 x 128 16-bit P tile
-  static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring slots
+  static constexpr int kPBytes = kPInTmem ? 0 : kBM * kBN * 2;  // one 128 x 128 16-bit P tile
+  static constexpr int kStages = (D == 128) ? 3 : 8;  // K/V ring slots
   static constexpr int kQOff = 0;
   static constexpr int kPOff = 2 * kTileBytes;
   static constexpr int kRingOff = kPOff + 2 * kPBytes;
@@ -302,15 +315,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_f16_ss(s_col, q_desc + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
           }
         };
+        // P_X in tensor memory (d = 64): lane = query row, column c holds keys
+        // (2c, 2c+1); a 16-key step of P.V reads 8 columns.
+        const uint32_t p_tcol = tmem + 2 * kBN + 2 * D + x * (kBN / 2);
         // P.V over keys [64 half, 64 half + 64): P column block `half`
         auto issue_pv_half = [&](int st, int half, bool accumulate) {
           const uint64_t vd = smem_desc_sw128(ring_addr + st * C::kTileBytes, C::kBlockBytes, 1024);
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
             const int kk = half * 4 + k4;
-            const uint64_t poff = (half * C::kBlockBytes + k4 * 32) >> 4;
-            mma_f16_ss(o_col, p_desc + poff, vd + ((kk * 2048) >> 4), kIdescPV,
-                       (accumulate || kk > 0) ? 1u : 0u);
+            const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+            if constexpr (C::kPInTmem) {
+              mma_f16_ts(o_col, p_tcol + kk * 8, vd + ((kk * 2048) >> 4), kIdescPV, acc);
+            } else {
+              const uint64_t poff = (half * C::kBlockBytes + k4 * 32) >> 4;
+              mma_f16_ss(o_col, p_desc + poff, vd + ((kk * 2048) >> 4), kIdescPV, acc);
+            }
           }
         };
         bool ok = nt == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
@@ -391,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // This row of P_X in shared memory: two 64-key column blocks of 128-byte
     // rows; 16-byte chunk c of the row sits at chunk c ^ (row % 8).
     uint8_t* p_row = sP + x * C::kPBytes + row * 128;
+    const uint32_t p_tmem = tmem + lane_off + 2 * kBN + 2 * D + x * (kBN / 2);  // d = 64
     const float lam = p.scale_log2;
     float r = -INFINITY;  // retained reference, raw score units
     float l = 0.f;
@@ -447,10 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l *= gamma;
       // ---- P = 2^(lambda*s - lambda*r), row sum, pack to 16 bits, and store
-      // the row of P_X(j) into shared memory (swizzled K-major A operand), one
-      // 64-key column block at a time: block 0 once PV_X(j-1) has read it,
-      // block 1 once PV_X(j-1) is complete (O_X is then stable, so the
-      // correction happens there too).
+      // the row of P_X(j) as the A operand of P.V (d = 128: shared memory,
+      // swizzled K-major; d = 64: this row's tensor-memory lane), one 64-key
+      // column block at a time: block 0 once PV_X(j-1) has read it, block 1
+      // once PV_X(j-1) is complete (O_X is then stable, so the correction
+      // happens there too).
       const float rs = (r == -INFINITY) ? 0.f : r * lam;
       const float2 lam2 = make_float2(lam, lam);
       const float2 nrs2 = make_float2(-rs, -rs);
@@ -476,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (C::kPInTmem) tc_fence_after();  // P.V(j-1) has read these columns: tcgen05.st may follow
           if (blk == kBN / 64 - 1) {
             tc_fence_after();
             // correction: O_row *= gamma (warp-uniform path; gamma = 1 rows unchanged)
@@ -494,16 +517,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if constexpr (C::kPInTmem) {
+          tmem_st32(p_tmem + blk * 32, pk);
+        } else {
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8)
-          *reinterpret_cast<uint4*>(p_row + blk * C::kBlockBytes + ((c8 ^ (row & 7)) << 4)) =
-              make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+          for (int c8 = 0; c8 < 8; ++c8)
+            *reinterpret_cast<uint4*>(p_row + blk * C::kBlockBytes + ((c8 ^ (row & 7)) << 4)) =
+                make_uint4(pk[c8 * 4], pk[c8 * 4 + 1], pk[c8 * 4 + 2], pk[c8 * 4 + 3]);
+        }
       }
       if (!ok) break;
       const float2 s01 = fadd2(fadd2(sum4[0], sum4[1]), fadd2(sum4[2], sum4[3]));
       l += s01.x + s01.y;
-      fence_proxy_async_smem();  // P stores -> visible to the tensor core (async proxy)
-      tc_fence_before();         // O correction (tcgen05.st) ordered before the arrive
+      if constexpr (C::kPInTmem) {
+        tmem_wait_st();            // P (tcgen05.st) complete before the arrive
+      } else {
+        fence_proxy_async_smem();  // P stores -> visible to the tensor core (async proxy)
+      }
+      tc_fence_before();           // P / O correction (tcgen05.st) ordered before the arrive
       mbar_arrive(&bars->p_full[x]);
     }
 
