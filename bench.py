@@ -792,9 +792,11 @@ def main():
     ap.add_argument("--fp8-only", action="store_true",
                     help="time only attn_fwd_fp8 on the headline forward workload (profiling runs)")
     ap.add_argument("--atomic", action="store_true",
-                    help="with --backward-only: time attn_bwd_atomic instead of attn_bwd")
+                    help="with --backward-only: time attn_bwd_atomic (already the default)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="with --backward-only: time attn_bwd (bitwise repeatable) instead of attn_bwd_atomic")
     ap.add_argument("--backward-only", action="store_true",
-                    help="time only attn_bwd on the headline forward workload (profiling runs)")
+                    help="time only the default backward (attn_bwd_atomic) on the headline forward workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-secondary", action="store_true", help="skip the second workload")
     ap.add_argument("--cta-pair", action="store_true",
@@ -841,7 +843,7 @@ def main():
         w2 = PREFILL if args.workload == "prefill" else WORKLOADS[args.workload]
         if args.batch > 0:
             w2 = with_batch(w2, args.batch)
-        line = bench_backward(args, world, rank, peaks, peak_kind, w=w2, atomic=args.atomic)
+        line = bench_backward(args, world, rank, peaks, peak_kind, w=w2, atomic=not args.deterministic)
         if rank == 0:
             print(json.dumps(line), flush=True)
         if world > 1:
@@ -861,10 +863,12 @@ def main():
             line["fp8"] = bench_fp8(args, world, rank, peaks, peak_kind, steps=max(3, min(args.steps, 20)),
                                     warmup=3)
             bw_steps = max(3, min(args.steps, 20))
+            # the default backward (attention_backward: attn_bwd_atomic), then the
+            # bitwise-repeatable one (attn_bwd)
             line["backward"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
-                                               warmup=3) for w2 in BACKWARD]
-            line["backward_atomic"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2, steps=bw_steps,
-                                                      warmup=3, atomic=True) for w2 in BACKWARD]
+                                               warmup=3, atomic=True) for w2 in BACKWARD]
+            line["backward_deterministic"] = [bench_backward(args, world, rank, peaks, peak_kind, w=w2,
+                                                             steps=bw_steps, warmup=3) for w2 in BACKWARD]
     elif args.workload in WORKLOADS and not WORKLOADS[args.workload].decode:
         w2 = WORKLOADS[args.workload]
         if args.batch > 0:
@@ -906,7 +910,7 @@ def main():
             line["fp8"]["cpu_baseline"] = dict(line["cpu_baseline"], sample=line["cpu_baseline"]["sample"]
                                                + " (the oracle takes the dequantized inputs at the same rate)")
         bwd_cpu = {}
-        for legs in (line.get("backward", []), line.get("backward_atomic", [])):
+        for legs in (line.get("backward", []), line.get("backward_deterministic", [])):
             for leg in legs:
                 if leg["workload"] not in bwd_cpu:
                     bwd_cpu[leg["workload"]] = cpu_line(*cpu_oracle_backward(WORKLOADS[leg["workload"]]),
@@ -926,9 +930,9 @@ def main():
         if isinstance(line.get("fp8"), dict):
             rows.append(leg_roofline(line["fp8"], "v_transpose_kernel + prefill_fp8_kernel"))
         for leg in line.get("backward", []):
-            rows.append(leg_roofline(leg, "attn_bwd (3 kernels)"))
-        for leg in line.get("backward_atomic", []):
-            rows.append(leg_roofline(leg, "attn_bwd_atomic (3 kernels)"))
+            rows.append(leg_roofline(leg, "attn_bwd_atomic (3 kernels; the default backward)"))
+        for leg in line.get("backward_deterministic", []):
+            rows.append(leg_roofline(leg, "attn_bwd (3 kernels; bitwise repeatable)"))
         if rows:
             line["roofline"]["legs"] = rows
     if rank == 0:

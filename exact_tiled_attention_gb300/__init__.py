@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     EXPORTS,
     GbattnError,
     LIB_PATH,
+    attention_backward,
     attn_bwd,
     attn_bwd_atomic,
     attn_bwd_atomic_workspace_bytes,

@@ -293,6 +293,18 @@ def attn_decode_splitkv_noalloc(q, k_cache, v_cache, seqlens, scale: float | Non
     return out, lse
 
 
+def attention_backward(q, k, v, o, lse, dout, scale: float | None = None, causal: bool = False,
+                       deterministic: bool = False, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """The backward a caller should use by default: attn_bwd_atomic (the
+    faster schedule in every measured case: five 128x128 products per
+    (query block, key tile) pair instead of seven), or attn_bwd when
+    `deterministic` asks for bitwise-repeatable dQ.  The workspace, if given,
+    must be sized by the matching *_workspace_bytes function."""
+    fn = attn_bwd if deterministic else attn_bwd_atomic
+    return fn(q, k, v, o, lse, dout, scale=scale, causal=causal, workspace=workspace, dq=dq, dk=dk, dv=dv,
+              stream=stream)
+
+
 def attn_fwd_fp8_workspace_bytes(B: int, Hkv: int, Sk: int, d: int) -> int:
     return int(load_library().attn_fwd_fp8_workspace_bytes(B, Hkv, Sk, d))
 

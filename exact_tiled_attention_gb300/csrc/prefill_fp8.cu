@@ -362,8 +362,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = half * 64 + w * 4;
           const float2 a = ffma2(make_float2(s[c], s[c + 1]), lam2, nrs2);
           const float2 e = ffma2(make_float2(s[c + 2], s[c + 3]), lam2, nrs2);
-          const float2 ta = make_float2(ex2_approx(a.x), ex2_approx(a.y));
-          const float2 te = make_float2(ex2_approx(e.x), ex2_approx(e.y));
+          // the build option GBATTN_EX2_EMU_EVERY sends every E-th pair to the
+          // FMA-pipe exp2 (ex2_pair), as in the 16-bit kernels
+          const float2 ta = ex2_pair(a, half * 32 + w * 2);
+          const float2 te = ex2_pair(e, half * 32 + w * 2 + 1);
           sum4[0] = fadd2(sum4[0], ta);
           sum4[1] = fadd2(sum4[1], te);
           pk[w] = pack4_e4m3(ta.x, ta.y, te.x, te.y);

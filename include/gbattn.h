@@ -198,6 +198,16 @@ int attn_decode_splitkv(const void *q, const void *k_cache, const void *v_cache,
                         int dtype, void *stream);
 
 /*
+ * Choosing a backward.  Two entry points compute the same gradients:
+ *   attn_bwd_atomic -- the default choice: faster in every measured case
+ *       (five 128 x 128 products per (query block, key tile) pair; dQ is
+ *       summed by fp32 atomic reductions, so its last bits may differ from
+ *       call to call; dK and dV repeat bitwise);
+ *   attn_bwd -- when dQ must repeat bitwise (one owner per output element,
+ *       seven products per pair).
+ */
+
+/*
  * attn_bwd_workspace_bytes -- bytes of device workspace attn_bwd needs: the
  * fp32 row scalars D [B, H, Sq] (rounded up to 256 bytes).  For B=1, H=32,
  * Sq=4096 this is the 0.5 MiB D entry of the scratch ledger in M4.4 0x06.1J;

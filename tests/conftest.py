@@ -23,3 +23,19 @@ def golden():
             return json.load(f)
 
     return load
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With GBATTN_GRAD_LOG set, write the measured gradient-error margins of
+    every backward comparison of the session to that file (JSON)."""
+    path = os.environ.get("GBATTN_GRAD_LOG")
+    if not path:
+        return
+    try:
+        from tests.parity_util import GRAD_LOG
+    except ImportError:
+        return
+    import json
+
+    with open(path, "w") as f:
+        json.dump(GRAD_LOG, f, indent=0)

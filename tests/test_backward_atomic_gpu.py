@@ -12,7 +12,7 @@ import oracle
 from exact_tiled_attention_gb300 import (GbattnError, attn_bwd, attn_bwd_atomic, attn_bwd_atomic_workspace_bytes,
                                          attn_fwd, gbattn_device_status)
 from exact_tiled_attention_gb300.inputs import WORKLOADS, make_generator, make_prefill, randn
-from tests.parity_util import assert_grad_close, host_f32
+from tests.parity_util import assert_grad_close, grad_extras, host_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -64,8 +64,9 @@ def test_bwd_atomic_small_all_elements(shape):
     scale = 1.0 / math.sqrt(d)
     dq, dk, dv = _fwd_bwd(q, k, v, do, scale, causal)
     rq, rk, rv, _, _ = oracle.attn_bwd(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, causal)
-    assert_grad_close(dq, rq, f"dq {shape}")
-    assert_grad_close(dk, rk, f"dk {shape}")
+    ex = grad_extras(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, causal)
+    assert_grad_close(dq, rq, f"dq {shape}", extra=ex["dq"])
+    assert_grad_close(dk, rk, f"dk {shape}", extra=ex["dk"])
     assert_grad_close(dv, rv, f"dv {shape}")
 
 
@@ -75,8 +76,9 @@ def test_bwd_atomic_scales(scale):
     do = _dout(q.shape, torch.bfloat16, 44)
     dq, dk, dv = _fwd_bwd(q, k, v, do, scale, True)
     rq, rk, rv, _, _ = oracle.attn_bwd(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, True)
-    assert_grad_close(dq, rq, f"dq scale {scale}")
-    assert_grad_close(dk, rk, f"dk scale {scale}")
+    ex = grad_extras(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, True)
+    assert_grad_close(dq, rq, f"dq scale {scale}", extra=ex["dq"])
+    assert_grad_close(dk, rk, f"dk scale {scale}", extra=ex["dk"])
     assert_grad_close(dv, rv, f"dv scale {scale}")
 
 
@@ -97,8 +99,11 @@ def test_bwd_atomic_workload_sampled_heads(name, kv_ids):
                                          w.causal, kv_ids)
     for r, kid in enumerate(kv_ids):
         b, kvh = divmod(kid, w.Hkv)
-        assert_grad_close(dq[b, kvh * g:(kvh + 1) * g], rq[r], f"{name} dq kv{kid}")
-        assert_grad_close(dk[b, kvh], rk[r], f"{name} dk kv{kid}")
+        grp = slice(kvh * g, (kvh + 1) * g)
+        ex = grad_extras(host_f32(q[b:b + 1, grp]), host_f32(k[b:b + 1, kvh:kvh + 1]), host_f32(v[b:b + 1, kvh:kvh + 1]),
+                         host_f32(do[b:b + 1, grp]), w.scale, w.causal)
+        assert_grad_close(dq[b, grp], rq[r], f"{name} dq kv{kid}", extra=ex["dq"][0])
+        assert_grad_close(dk[b, kvh], rk[r], f"{name} dk kv{kid}", extra=ex["dk"][0, 0])
         assert_grad_close(dv[b, kvh], rv[r], f"{name} dv kv{kid}")
 
 

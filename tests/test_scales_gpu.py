@@ -12,7 +12,7 @@ from exact_tiled_attention_gb300 import (attn_bwd, attn_decode_splitkv, attn_fwd
                                          gbattn_device_status)
 from exact_tiled_attention_gb300.inputs import make_generator, make_prefill, randn
 from tests.fp8_util import oracle_fp8, quantize_per_kv_head
-from tests.parity_util import assert_attn_close, assert_grad_close, host_f32
+from tests.parity_util import assert_attn_close, assert_grad_close, grad_extras, host_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -50,8 +50,9 @@ def test_backward_scales(scale, d, dt, causal):
     torch.cuda.synchronize()
     assert gbattn_device_status() == 0
     rq, rk, rv, _, _ = oracle.attn_bwd(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, causal)
-    assert_grad_close(dq, rq, f"dq scale {scale} d {d}")
-    assert_grad_close(dk, rk, f"dk scale {scale} d {d}")
+    ex = grad_extras(host_f32(q), host_f32(k), host_f32(v), host_f32(do), scale, causal)
+    assert_grad_close(dq, rq, f"dq scale {scale} d {d}", extra=ex["dq"])
+    assert_grad_close(dk, rk, f"dk scale {scale} d {d}", extra=ex["dk"])
     assert_grad_close(dv, rv, f"dv scale {scale} d {d}")
 
 
