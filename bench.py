@@ -129,6 +129,14 @@ def kernel_source_hash(files) -> str:
 
 PREFILL_SOURCES = ["exact_tiled_attention_gb300/csrc/prefill_fwd.cu",
                    "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]
+PAIR_SOURCES = ["exact_tiled_attention_gb300/csrc/prefill_pair.cu",
+                "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]
+FP8_SOURCES = ["exact_tiled_attention_gb300/csrc/prefill_fp8.cu",
+               "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]
+BWD_SOURCES = {True: ["exact_tiled_attention_gb300/csrc/backward_atomic.cu",
+                      "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"],
+               False: ["exact_tiled_attention_gb300/csrc/backward.cu",
+                       "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]}
 DECODE_SOURCES = ["exact_tiled_attention_gb300/csrc/decode_splitkv.cu",
                   "exact_tiled_attention_gb300/csrc/gbattn_ptx.cuh"]
 
@@ -336,7 +344,7 @@ def bench_prefill(args, world, rank, peaks, peak_kind, w=None, with_e2e=True, pa
     key += ("causal>" if w.causal else "noncausal>") + ("" if w is PREFILL else f"@{w.name}")
     if pair:
         key = f"prefill_pair_kernel<{'bf16' if w.dtype == torch.bfloat16 else 'fp16'}>@{w.name}"
-    traffic = ncu_traffic(key, PREFILL_SOURCES, w.name)
+    traffic = ncu_traffic(key, PAIR_SOURCES if pair else PREFILL_SOURCES, w.name)
     dtype_name = "bf16" if w.dtype == torch.bfloat16 else "fp16"
     if not with_e2e:
         return {"workload": w.name, "impl": "cta_pair" if pair else "one_cta", "value": round(tflops_job, 3),
@@ -563,7 +571,9 @@ def bench_backward(args, world, rank, peaks, peak_kind, w=None, steps=None, warm
             "flops_per_call": flops, "flop_convention": "2.5 x forward (10*B*H*Sq*Sk*d, /2 causal)",
             "kernels_per_call": 3,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak,
-                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic(f"{'attn_bwd_atomic' if atomic else 'attn_bwd'} call@{w.name}",
+                                                BWD_SOURCES[atomic], w.name),
                          "peak_kind": f"{peak_kind} bf16 burst; time of all three kernels"},
             "l2": l2_note, "clocks": clocks}
 
@@ -612,7 +622,8 @@ def bench_fp8(args, world, rank, peaks, peak_kind, w=None, steps=None, warmup=No
             "ms_per_call": round(per_call * 1e3, 4), "steps": steps, "warmup": warmup, "dtype": "e4m3",
             "flops_per_call": flops, "kernels_per_call": 2,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "frac": round(achieved / peak, 4),
+                         "traffic": ncu_traffic(f"attn_fwd_fp8 call@{w.name}_e4m3", FP8_SOURCES, w.name),
                          "peak_kind": f"{peak_kind} bf16 burst x 2 (dense FP8 : BF16 = 2); "
                                       "V transpose included"},
             "l2": "inputs 256 MiB per call > 129 MB L2; no flush", "clocks": clocks}
