@@ -41,6 +41,8 @@ def _run_and_compare(B, H, Hkv, Sq, Sk, d, dt, causal, seed):
     (1, 2, 2, 129, 700, 128, "fp16", False),
     (1, 3, 1, 512, 512, 128, "bf16", True),
     (1, 2, 2, 640, 640, 128, "fp16", True),
+    (2, 4, 2, 700, 700, 64, "fp16", True),   # d = 64: several query pairs, GQA g = 2, diagonal tiles
+    (1, 3, 3, 1100, 900, 64, "bf16", False), # d = 64: Sq != Sk, ragged key tail
     # rectangular causal, bottom-right: Sq < Sk and Sq > Sk (rows with no key)
     (1, 2, 2, 64, 1000, 128, "bf16", True),
     (1, 2, 1, 200, 77, 64, "bf16", True),
