@@ -955,7 +955,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const uint16_t* __r
 int head_group_for(long long per_head_bytes, long long heads) {
   long long hg = (48LL << 20) / (per_head_bytes > 0 ? per_head_bytes : 1);
   if (hg < 1) hg = 1;
-  return static_cast<int>(hg < heads ? hg : heads);
+  return balanced_head_group(hg, heads, 1);
 }
 
 template <int D, bool BF16, bool CAUSAL>

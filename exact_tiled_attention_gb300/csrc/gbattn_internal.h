@@ -116,6 +116,26 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn encode_tiled_fn();
 
+// Heads per L2 scheduling group.  The launchers order their CTAs in groups of
+// heads whose K/V (or whatever per-head data the kernel re-reads) stay resident
+// in L2 while the group runs: at most hg_max heads, a multiple of `step` (whole
+// KV-head groups), and groups of equal size -- the largest such size, down to
+// half of hg_max, that divides `heads`, else near-equal groups.  A short last
+// group would start its heaviest (causal) units last and leave a tail: at 64
+// heads of 4 MB, groups of 12 (five of 12, one of 4) measured 5 % slower on the
+// causal 8192-token forward than groups of 8.
+inline int balanced_head_group(long long hg_max, long long heads, long long step) {
+  if (step < 1) step = 1;
+  if (hg_max < step) hg_max = step;
+  if (hg_max > heads) hg_max = heads;
+  for (long long c = hg_max - hg_max % step; c >= step && 2 * c >= hg_max; c -= step)
+    if (heads % c == 0) return static_cast<int>(c);
+  const long long n_groups = (heads + hg_max - 1) / hg_max;
+  long long hg = (heads + n_groups - 1) / n_groups;
+  hg = (hg + step - 1) / step * step;
+  return static_cast<int>(hg < heads ? hg : heads);
+}
+
 // Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
 // device, once per device for each call site (`done` holds one bit per device
 // ordinal; devices past 63 set it on every call).  The attribute belongs to

@@ -522,8 +522,7 @@ int launch_fp8_t(const PrefillFp8Args& a) {
     const long long kv_head_bytes = 2LL * a.Sk * kD;
     long long kv_heads = (48LL << 20) / (kv_head_bytes > 0 ? kv_head_bytes : 1);
     if (kv_heads < 1) kv_heads = 1;
-    const long long hg = kv_heads * p.g, BH = static_cast<long long>(a.B) * a.H;
-    p.head_group = static_cast<int>(hg < BH ? hg : BH);
+    p.head_group = balanced_head_group(kv_heads * p.g, static_cast<long long>(a.B) * a.H, p.g);
   }
   p.delta = a.Sk - a.Sq;
   p.scale = a.scale;

@@ -549,12 +549,12 @@ int launch_pair_t(const PrefillArgs& a) {
   p.g = a.H / a.Hkv;
   p.n_quads = (a.Sq + 4 * kBM - 1) / (4 * kBM);
   {
-    // Heads per scheduling group: about 48 MB of K/V in flight (L2 is 129 MB).
+    // Heads per scheduling group: about 48 MB of K/V in flight (L2 is 129 MB),
+    // whole KV-head groups, groups of equal size (balanced_head_group).
     const long long kv_head_bytes = 4LL * a.Sk * kD;  // K and V, 16-bit
     long long kv_heads = (48LL << 20) / (kv_head_bytes > 0 ? kv_head_bytes : 1);
     if (kv_heads < 1) kv_heads = 1;
-    const long long hg = kv_heads * p.g, BH = static_cast<long long>(a.B) * a.H;
-    p.head_group = static_cast<int>(hg < BH ? hg : BH);
+    p.head_group = balanced_head_group(kv_heads * p.g, static_cast<long long>(a.B) * a.H, p.g);
   }
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
