@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     gbattn_causal_tile_counts,
     gbattn_device_status,
     gbattn_selftest_bounded_wait,
+    gbattn_timeline_set,
     gbattn_exp2_paths,
     gbattn_version,
     load_library,

@@ -32,8 +32,8 @@ EXPORTS = ("attn_fwd", "attn_fwd_pair", "attn_decode_workspace_bytes", "attn_dec
            "attn_bwd_workspace_bytes", "attn_bwd", "attn_bwd_atomic_workspace_bytes", "attn_bwd_atomic",
            "gbattn_exp2_paths",
            "attn_fwd_fp8_workspace_bytes", "attn_fwd_fp8", "gbattn_selftest_bounded_wait",
-           "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_error_string",
-           "gbattn_version")
+           "gbattn_causal_tile_counts", "gbattn_device_status", "gbattn_timeline_set",
+           "gbattn_error_string", "gbattn_version")
 
 _lock = threading.Lock()
 _lib = None
@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.gbattn_causal_tile_counts.restype = ci
         lib.gbattn_selftest_bounded_wait.argtypes = [ci, vp]
         lib.gbattn_selftest_bounded_wait.restype = ci
+        lib.gbattn_timeline_set.argtypes = [vp, ctypes.c_longlong]
+        lib.gbattn_timeline_set.restype = ci
         lib.gbattn_device_status.argtypes = []
         lib.gbattn_device_status.restype = ci
         lib.gbattn_error_string.argtypes = [ci]
@@ -444,6 +446,32 @@ def gbattn_selftest_bounded_wait(arrive: bool, stream=None) -> None:
     rc = load_library().gbattn_selftest_bounded_wait(int(bool(arrive)), _stream_ptr(stream))
     if rc != GBATTN_OK:
         raise GbattnError(rc, "gbattn_selftest_bounded_wait")
+
+
+_timeline_records = None  # keeps the buffer alive while the library holds its address
+
+
+def gbattn_timeline_set(records) -> None:
+    """Per-CTA timeline of attn_fwd launches: `records` is an int64 CUDA tensor
+    of shape [capacity, 4] (start ns, end ns, SM, unit per CTA; see the header),
+    or None to turn the timeline off.  A launch with more CTAs than
+    `capacity` records nothing."""
+    global _timeline_records
+    lib = load_library()
+    if records is None:
+        rc = lib.gbattn_timeline_set(None, 0)
+        if rc != GBATTN_OK:
+            raise GbattnError(rc, "gbattn_timeline_set")
+        _timeline_records = None
+        return
+    if not isinstance(records, torch.Tensor) or not records.is_cuda:
+        raise ValueError("timeline records must be a CUDA tensor")
+    if records.dtype != torch.int64 or records.dim() != 2 or records.shape[1] != 4 or not records.is_contiguous():
+        raise ValueError("timeline records must be a contiguous int64 tensor of shape [capacity, 4]")
+    rc = lib.gbattn_timeline_set(ctypes.c_void_p(records.data_ptr()), int(records.shape[0]))
+    if rc != GBATTN_OK:
+        raise GbattnError(rc, "gbattn_timeline_set")
+    _timeline_records = records
 
 
 def gbattn_device_status() -> int:

@@ -27,12 +27,19 @@ int* g_status_ptr[kMaxDevices] = {};
 unsigned long long g_status_ctx[kMaxDevices] = {};
 int g_sm_major[kMaxDevices] = {};
 int g_sm_minor[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
 std::mutex g_dev_mutex;
+
+// Per-CTA timeline of attn_fwd launches (gbattn_timeline_set).
+std::mutex g_timeline_mutex;
+unsigned long long* g_timeline = nullptr;
+long long g_timeline_capacity = 0;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Returns GBATTN_OK and the status pointer of the current device, or an error.
-int current_device(int** status) {
+// Returns GBATTN_OK and the status pointer (and, if asked, the SM count) of
+// the current device, or an error.
+int current_device(int** status, int* sm_count = nullptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -41,14 +48,16 @@ int current_device(int** status) {
   const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   if (g_status_ptr[dev] == nullptr || ctx != g_status_ctx[dev]) {
-    int major = 0, minor = 0;
+    int major = 0, minor = 0, sms = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
       cudaGetLastError();
       return GBATTN_EUNSUPPORTED;
     }
     g_sm_major[dev] = major;
     g_sm_minor[dev] = minor;
+    g_sm_count[dev] = sms;
     if (major != 10 || minor != 3) return GBATTN_EUNSUPPORTED;
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) {
@@ -60,6 +69,7 @@ int current_device(int** status) {
   }
   if (g_sm_major[dev] != 10 || g_sm_minor[dev] != 3) return GBATTN_EUNSUPPORTED;
   *status = g_status_ptr[dev];
+  if (sm_count != nullptr) *sm_count = g_sm_count[dev];
   return GBATTN_OK;
 }
 
@@ -200,9 +210,10 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (static_cast<long long>(B) * H > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
     return GBATTN_EBADSHAPE;
   int* status = nullptr;
-  int rc = current_device(&status);
+  int sms = 0;
+  int rc = current_device(&status, &sms);
   if (rc != GBATTN_OK) return rc;
-  PrefillArgs a;
+  PrefillArgs a{};
   a.q = q;
   a.k = k;
   a.v = v;
@@ -219,6 +230,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.bf16 = dtype == GBATTN_BF16;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = status;
+  a.num_sms = sms;
+  {
+    std::lock_guard<std::mutex> lock(g_timeline_mutex);
+    a.timeline = g_timeline;
+    a.timeline_capacity = g_timeline_capacity;
+  }
   return launch_prefill(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 
@@ -236,7 +253,7 @@ int attn_fwd_pair(const void* q, const void* k, const void* v, void* o, float* l
   int* status = nullptr;
   int rc = current_device(&status);
   if (rc != GBATTN_OK) return rc;
-  PrefillArgs a;
+  PrefillArgs a{};
   a.q = q;
   a.k = k;
   a.v = v;
@@ -517,6 +534,17 @@ int gbattn_selftest_bounded_wait(int arrive, void* stream) {
   if (rc != GBATTN_OK) return rc;
   selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(arrive ? 1 : 0, status);
   return cudaGetLastError() == cudaSuccess ? GBATTN_OK : GBATTN_ELAUNCH;
+}
+
+int gbattn_timeline_set(unsigned long long* records, long long capacity) {
+  if (records != nullptr) {
+    if ((reinterpret_cast<uintptr_t>(records) & 7u) != 0) return GBATTN_EPOINTER;
+    if (capacity < 1) return GBATTN_EBADSHAPE;
+  }
+  std::lock_guard<std::mutex> lock(g_timeline_mutex);
+  g_timeline = records;
+  g_timeline_capacity = records != nullptr ? capacity : 0;
+  return GBATTN_OK;
 }
 
 int gbattn_device_status(void) {

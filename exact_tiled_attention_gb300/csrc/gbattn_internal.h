@@ -23,7 +23,10 @@ struct PrefillArgs {
   int causal;
   bool bf16;
   cudaStream_t stream;
-  int* status;  // device status word
+  int* status;                     // device status word
+  int num_sms;                     // SMs of the device (CTAs resident at once)
+  unsigned long long* timeline;    // per-CTA records (gbattn_timeline_set), or null
+  long long timeline_capacity;     // records the buffer holds
 };
 
 // Arguments of one split-KV decode (partial + merge) launch.

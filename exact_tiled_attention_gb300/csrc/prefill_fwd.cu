@@ -109,6 +109,8 @@ struct Params {
   float scale_log2;
   int causal;
   int* status;
+  int wave;                       // CTAs resident at once (one per SM)
+  unsigned long long* timeline;   // optional per-CTA records, or null
 };
 
 struct __align__(8) Barriers {
@@ -164,6 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  unsigned long long t_start = 0;
+  if (p.timeline != nullptr && threadIdx.x == 0) t_start = global_timer_ns();
 
   // ---- work unit.  CTAs are ordered in groups of p.head_group (batch, head)
   // pairs so that the K/V of the heads in flight stay resident in L2; inside
@@ -235,6 +239,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t keep = policy_evict_last();  // K/V: re-read by other CTAs
     pre_issued = min(C::kStages, n_items);
     for (int it = 0; it < pre_issued; ++it) issue_item(it, keep);
+    // Q of the unit one wave ahead (the CTA that will most likely start on
+    // an SM when the current wave drains) into L2, so that its first load
+    // is not an HBM round trip.
+    const int ahead = blockIdx.x + p.wave;
+    if (ahead < static_cast<int>(gridDim.x)) {
+      const int ga = ahead / (p.head_group * p.n_pairs);
+      const int heads_a = min(p.head_group, BH - ga * p.head_group);
+      const int ra = ahead - ga * p.head_group * p.n_pairs;
+      const int bh_a = ga * p.head_group + ra % heads_a;
+      const int pair_a = p.n_pairs - 1 - ra / heads_a;
+      for (int x = 0; x < 2; ++x) {
+        const int qa = (2 * pair_a + x) * kBM;
+        if (qa >= p.Sq) continue;
+        for (int cb = 0; cb < C::kColBlocks; ++cb) tma_prefetch_l2_3d(&tmap_q, cb * 64, qa, bh_a);
+      }
+    }
   }
   if (threadIdx.x == 0) {
     for (int x = 0; x < 2; ++x) {
@@ -548,70 +568,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool row_ok = q_row < p.Sq;
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      // d = 64 (measured faster): O_X is staged in Q_X (dead since QK_X of the
-      // last key tile completed) and written by TMA; d = 128 (measured faster
-      // this way): each thread stores its row directly.
-      if constexpr (D == 64) {
-        // O_X is staged in Q_X (dead since QK_X of the last key tile completed)
-        // in the Q layout -- 64-element column blocks of 128-byte rows, 16-byte
-        // chunk c at chunk c ^ (row % 8) -- and written by one TMA store per
-        // column block (rows past Sq are not written).
-        uint8_t* o_row = sQ + x * C::kTileBytes + row * 128;
+      // O_X is staged in Q_X (dead since QK_X of the last key tile completed)
+      // in the Q layout -- 64-element column blocks of 128-byte rows, 16-byte
+      // chunk c at chunk c ^ (row % 8) -- and written by one TMA store per
+      // column block (rows past Sq are not written).  Each thread storing its
+      // own row to global memory instead costs one cache line per lane and
+      // store instruction: ~4,000 line writes per CTA, ~1.8 us (traced).
+      uint8_t* o_row = sQ + x * C::kTileBytes + row * 128;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          if (have_o) {
-            tmem_ld32(o_tmem + c * 32, u);
-            tmem_wait_ld();
-            reg_fence32(u);
-          } else {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (have_o) {
+          tmem_ld32(o_tmem + c * 32, u);
+          tmem_wait_ld();
+          reg_fence32(u);
+        } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = 0u;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
-          uint8_t* blk = o_row + (c / 2) * C::kBlockBytes;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int ch = (c % 2) * 4 + k;
-            *reinterpret_cast<uint4*>(blk + ((ch ^ (row & 7)) << 4)) =
-                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-          }
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
         }
-        fence_proxy_async_smem();    // O stores -> visible to the TMA engine
-        named_bar_sync(1 + x, kBM);  // the four warps of the tile have written O_X
-        if (wq == 0 && lane == 0) {
-          for (int cb = 0; cb < C::kColBlocks; ++cb)
-            tma_store_3d(&tmap_o, sQ + x * C::kTileBytes + cb * C::kBlockBytes, cb * 64, q0x, b * p.H + h);
-          bulk_commit_group();
-          bulk_wait_group_read0();  // shared memory read before the CTA may exit
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
+        uint8_t* blk = o_row + (c / 2) * C::kBlockBytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int ch = (c % 2) * 4 + k;
+          *reinterpret_cast<uint4*>(blk + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
-      } else {
-        using T = uint16_t;
-        T* orow = reinterpret_cast<T*>(p.o) + ((static_cast<size_t>(b) * p.H + h) * p.Sq + (row_ok ? q_row : 0)) * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t u[32];
-          if (have_o) {
-            tmem_ld32(o_tmem + c * 32, u);
-            tmem_wait_ld();
-            reg_fence32(u);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) u[i] = 0u;
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack2<BF16>(__uint_as_float(u[2 * i]) * inv, __uint_as_float(u[2 * i + 1]) * inv);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
+      }
+      fence_proxy_async_smem();    // O stores -> visible to the TMA engine
+      named_bar_sync(1 + x, kBM);  // the four warps of the tile have written O_X
+      if (wq == 0 && lane == 0) {
+        for (int cb = 0; cb < C::kColBlocks; ++cb)
+          tma_store_3d(&tmap_o, sQ + x * C::kTileBytes + cb * C::kBlockBytes, cb * 64, q0x, b * p.H + h);
+        bulk_commit_group();
+        bulk_wait_group_read0();  // shared memory read before the CTA may exit
       }
       if (row_ok && p.lse != nullptr) {
         const float lse = (l > 0.f) ? (r * lam + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -624,6 +617,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (p.timeline != nullptr && threadIdx.x == 0) {
+    // Timeline record of this CTA: start and end (%globaltimer ns), SM, unit.
+    unsigned long long* rec = p.timeline + 4 * static_cast<size_t>(blockIdx.x);
+    rec[0] = t_start;
+    rec[1] = global_timer_ns();
+    rec[2] = sm_id();
+    rec[3] = static_cast<unsigned long long>(bh) << 32 | static_cast<unsigned>(pair);
+  }
   if (warp == kMmaWarpH) tmem_dealloc(tmem, 512);
 }
 
@@ -639,7 +640,7 @@ int launch_t(const PrefillArgs& a) {
   auto kern = prefill_fwd_kernel<D, BF16, CAUSAL>;
   static std::atomic<unsigned long long> attr_done{0};  // per instantiation
   if (!set_smem_limit_once(kern, C::kSmemBytes, attr_done)) return -1;
-  Params p;
+  Params p{};
   p.o = a.o;
   p.lse = a.lse;
   p.B = a.B;
@@ -661,8 +662,10 @@ int launch_t(const PrefillArgs& a) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.causal = CAUSAL ? 1 : 0;
   p.status = a.status;
+  p.wave = a.num_sms;
   const long long grid = static_cast<long long>(a.B) * a.H * p.n_pairs;
   if (grid > 0x7FFFFFFFLL) return -1;
+  p.timeline = (a.timeline != nullptr && a.timeline_capacity >= grid) ? a.timeline : nullptr;
   kern<<<static_cast<unsigned>(grid), kThreads, C::kSmemBytes, a.stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

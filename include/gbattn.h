@@ -381,6 +381,25 @@ int gbattn_selftest_bounded_wait(int arrive, void *stream);
  */
 int gbattn_device_status(void);
 
+/*
+ * gbattn_timeline_set -- per-CTA timeline of attn_fwd launches (a profiling
+ * aid; the method has no counterpart).  While set, every attn_fwd launch
+ * whose grid has at most `capacity` CTAs writes, for CTA i, four unsigned
+ * 64-bit values at records[4 i .. 4 i + 3]:
+ *   [0] start and [1] end of the CTA, in %globaltimer nanoseconds,
+ *   [2] the SM it ran on,
+ *   [3] its work unit, (b * H + h) << 32 | query pair (rows 256 p .. 256 p + 255).
+ * A launch with more CTAs than `capacity` writes nothing.  The grid of a
+ * launch has B * H * ceil(Sq / 256) CTAs.  records is a device pointer owned
+ * by the caller, 8-byte aligned, at least 32 * capacity bytes, and must stay
+ * valid until the launches that write it have completed.  records = NULL
+ * turns the timeline off (capacity is then ignored).  The setting is
+ * process-wide and is read when a launch is enqueued.
+ * Errors: GBATTN_EPOINTER (records not 8-byte aligned), GBATTN_EBADSHAPE
+ * (records != NULL and capacity < 1).
+ */
+int gbattn_timeline_set(unsigned long long *records, long long capacity);
+
 /* Text for a status code (static storage; never NULL). */
 const char *gbattn_error_string(int code);
 

@@ -290,3 +290,22 @@ def test_decode_wrappers_reject_mismatched_tensors(wrapper):
         a.update(over)
         with pytest.raises(exc):
             fn(a["q"], a["k"], a["v"], a["sl"], out=a["out"], lse=a["lse"])
+
+
+def test_timeline_set_validation(lib):
+    """gbattn_timeline_set checks alignment and capacity on the host, and
+    NULL turns the timeline off whatever the capacity."""
+    try:
+        assert lib.gbattn_timeline_set(FAKE + 4, 16) == -5     # not 8-byte aligned
+        assert lib.gbattn_timeline_set(FAKE, 0) == -1
+        assert lib.gbattn_timeline_set(FAKE, -3) == -1
+        assert lib.gbattn_timeline_set(None, -3) == 0
+        assert lib.gbattn_timeline_set(FAKE, 8) == 0
+    finally:
+        assert lib.gbattn_timeline_set(None, 0) == 0
+
+
+def test_timeline_wrapper_rejects_bad_buffers():
+    with pytest.raises(ValueError):
+        binding.gbattn_timeline_set(torch.zeros(8, 4, dtype=torch.int64))           # not CUDA
+    binding.gbattn_timeline_set(None)
