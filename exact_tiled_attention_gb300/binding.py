@@ -452,7 +452,7 @@ _timeline_records = None  # keeps the buffer alive while the library holds its a
 
 
 def gbattn_timeline_set(records) -> None:
-    """Per-CTA timeline of attn_fwd launches: `records` is an int64 CUDA tensor
+    """Per-CTA timeline of attn_fwd and attn_fwd_fp8 launches: `records` is an int64 CUDA tensor
     of shape [capacity, 4] (start ns, end ns, SM, unit per CTA; see the header),
     or None to turn the timeline off.  A launch with more CTAs than
     `capacity` records nothing."""

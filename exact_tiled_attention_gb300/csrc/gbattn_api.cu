@@ -433,9 +433,10 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* q_des
     return GBATTN_EBADSHAPE;
   if (workspace_bytes < attn_fwd_fp8_workspace_bytes(B, Hkv, Sk, d)) return GBATTN_EWORKSPACE;
   int* status = nullptr;
-  int rc = current_device(&status);
+  int sms = 0;
+  int rc = current_device(&status, &sms);
   if (rc != GBATTN_OK) return rc;
-  PrefillFp8Args a;
+  PrefillFp8Args a{};
   a.q = q;
   a.k = k;
   a.v = v;
@@ -455,6 +456,12 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* q_des
   a.vt = workspace;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = status;
+  a.num_sms = sms;
+  {
+    std::lock_guard<std::mutex> lock(g_timeline_mutex);
+    a.timeline = g_timeline;
+    a.timeline_capacity = g_timeline_capacity;
+  }
   return launch_prefill_fp8(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 

@@ -83,6 +83,9 @@ struct PrefillFp8Args {
   void* vt;        // workspace: E4M3 [B,Hkv,d,Sk_pad], Sk_pad = Sk rounded up to 128
   cudaStream_t stream;
   int* status;
+  int num_sms;                     // SMs of the device (CTAs resident at once)
+  unsigned long long* timeline;    // per-CTA records (gbattn_timeline_set), or null
+  long long timeline_capacity;     // records the buffer holds
 };
 
 // Each returns a cudaError_t / CUresult folded into 0 (ok) or -1 (launch or

@@ -73,6 +73,8 @@ struct Fp8Params {
   int n_pairs, head_group, delta;
   float scale;
   int* status;
+  int wave;                       // CTAs resident at once (one per SM)
+  unsigned long long* timeline;   // optional per-CTA records, or null
 };
 
 struct __align__(8) Bars {
@@ -107,7 +109,8 @@ __device__ __forceinline__ int item_of_v(int j, int n) { return j <= n - 2 ? 2 *
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fp8_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                       const __grid_constant__ CUtensorMap tmap_vt, const Fp8Params p) {
+                       const __grid_constant__ CUtensorMap tmap_vt, const __grid_constant__ CUtensorMap tmap_o,
+                       const Fp8Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -118,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  unsigned long long t_start = 0;
+  if (p.timeline != nullptr && threadIdx.x == 0) t_start = global_timer_ns();
 
   // ---- work unit (same order as the 16-bit forward): groups of heads whose
   // K/V stay in L2, heaviest causal query pairs first, heads fastest.
@@ -178,6 +183,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&bars->q_full, (nt_h > 0 ? kTile : 0) + (nt_l > 0 ? kTile : 0));
         if (nt_h > 0) tma_load_3d(sQ, &tmap_q, &bars->q_full, 0, q0_h, b * p.H + h, once);
         if (nt_l > 0) tma_load_3d(sQ + kTile, &tmap_q, &bars->q_full, 0, q0_l, b * p.H + h, once);
+        {  // Q of the unit one wave ahead into L2 (as in the 16-bit forward)
+          const int ahead = blockIdx.x + p.wave;
+          if (ahead < static_cast<int>(gridDim.x)) {
+            const int ga = ahead / (p.head_group * p.n_pairs);
+            const int heads_a = min(p.head_group, BH - ga * p.head_group);
+            const int ra = ahead - ga * p.head_group * p.n_pairs;
+            const int bh_a = ga * p.head_group + ra % heads_a;
+            const int pair_a = p.n_pairs - 1 - ra / heads_a;
+            for (int x = 0; x < 2; ++x) {
+              const int qa = (2 * pair_a + x) * kBM;
+              if (qa < p.Sq) tma_prefetch_l2_3d(&tmap_q, 0, qa, bh_a);
+            }
+          }
+        }
         const int n_items = 2 * n_max;
         int issued = 0;
         for (int it = 0; it < n_items; ++it) {
@@ -420,8 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool row_ok = q_row < p.Sq;
       const float mul = (l > 0.f) ? dvs / l : 0.f;
-      uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) +
-                       ((static_cast<size_t>(b) * p.H + h) * p.Sq + (row_ok ? q_row : 0)) * kD;
+      // O_X (bf16, two 64-column blocks of 16 KiB) is staged in Q_X and P_X
+      // (dead once the last P.V has completed), 128-byte rows with 16-byte
+      // chunk c at chunk c ^ (row % 8), and written by two TMA stores (rows
+      // past Sq are not written).
 #pragma unroll 1
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t w[32];
@@ -437,11 +458,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack2<true>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        uint8_t* blk = ((c / 2) ? sP : sQ) + x * kTile + row * 128;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int k = 0; k < 4; ++k) {
+          const int ch = (c % 2) * 4 + k;
+          *reinterpret_cast<uint4*>(blk + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + x, kBM);
+      if (wq == 0 && lane == 0) {
+        tma_store_3d(&tmap_o, sQ + x * kTile, 0, q0x, b * p.H + h);
+        tma_store_3d(&tmap_o, sP + x * kTile, 64, q0x, b * p.H + h);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
       if (row_ok && p.lse != nullptr) {
         const float lse = (l > 0.f) ? (r * lam + __log2f(l) - kOmega) * 0.69314718055994531f : -INFINITY;
@@ -453,6 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (p.timeline != nullptr && threadIdx.x == 0) {
+    unsigned long long* rec = p.timeline + 4 * static_cast<size_t>(blockIdx.x);
+    rec[0] = t_start;
+    rec[1] = global_timer_ns();
+    rec[2] = sm_id();
+    rec[3] = static_cast<unsigned long long>(bh) << 32 | static_cast<unsigned>(pair);
+  }
   if (warp == kMmaWarpH) tmem_dealloc(tmem, 512);
 }
 
@@ -496,15 +534,16 @@ int launch_fp8_t(const PrefillFp8Args& a) {
   if (BHkv > 65535) return -1;
   v_transpose_kernel<<<dim3(Sk_pad / 64, static_cast<unsigned>(BHkv)), 256, 0, a.stream>>>(
       static_cast<const uint8_t*>(a.v), static_cast<uint8_t*>(a.vt), a.Sk, Sk_pad);
-  CUtensorMap tq, tk, tvt;
+  CUtensorMap tq, tk, tvt, to;
   if (!make_tmap_3d_u8(&tq, a.q, kD, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
       !make_tmap_3d_u8(&tk, a.k, kD, a.Sk, BHkv, kBN) ||
-      !make_tmap_3d_u8(&tvt, a.vt, Sk_pad, kD, BHkv, kD))
+      !make_tmap_3d_u8(&tvt, a.vt, Sk_pad, kD, BHkv, kD) ||
+      !make_tmap_3d(&to, a.o, true, kD, a.Sq, static_cast<long long>(a.B) * a.H, kBM))
     return -1;
   auto kern = prefill_fp8_kernel<CAUSAL>;
   static std::atomic<unsigned long long> attr_done{0};  // per instantiation
   if (!set_smem_limit_once(kern, kSmemBytes, attr_done)) return -1;
-  Fp8Params p;
+  Fp8Params p{};
   p.o = a.o;
   p.lse = a.lse;
   p.dq = a.q_descale;
@@ -527,9 +566,11 @@ int launch_fp8_t(const PrefillFp8Args& a) {
   p.delta = a.Sk - a.Sq;
   p.scale = a.scale;
   p.status = a.status;
+  p.wave = a.num_sms;
   const long long grid = static_cast<long long>(a.B) * a.H * p.n_pairs;
   if (grid > 0x7FFFFFFFLL) return -1;
-  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(tq, tk, tvt, p);
+  p.timeline = (a.timeline != nullptr && a.timeline_capacity >= grid) ? a.timeline : nullptr;
+  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(tq, tk, tvt, to, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -382,10 +382,10 @@ int gbattn_selftest_bounded_wait(int arrive, void *stream);
 int gbattn_device_status(void);
 
 /*
- * gbattn_timeline_set -- per-CTA timeline of attn_fwd launches (a profiling
- * aid; the method has no counterpart).  While set, every attn_fwd launch
- * whose grid has at most `capacity` CTAs writes, for CTA i, four unsigned
- * 64-bit values at records[4 i .. 4 i + 3]:
+ * gbattn_timeline_set -- per-CTA timeline of attn_fwd and attn_fwd_fp8
+ * launches (a profiling aid; the method has no counterpart).  While set,
+ * every such launch whose grid has at most `capacity` CTAs writes, for CTA
+ * i, four unsigned 64-bit values at records[4 i .. 4 i + 3]:
  *   [0] start and [1] end of the CTA, in %globaltimer nanoseconds,
  *   [2] the SM it ran on,
  *   [3] its work unit, (b * H + h) << 32 | query pair (rows 256 p .. 256 p + 255).

@@ -1,4 +1,4 @@
-"""GPU: the per-CTA timeline of attn_fwd (gbattn_timeline_set).  Each CTA of
+"""GPU: the per-CTA timeline of attn_fwd and attn_fwd_fp8 (gbattn_timeline_set).  Each CTA of
 a launch writes one record (start, end, SM, work unit); the units of one
 launch cover every (batch, head, query pair) exactly once, and the output
 with the timeline on still matches the fp64 oracle."""
@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from exact_tiled_attention_gb300 import attn_fwd, gbattn_device_status, gbattn_timeline_set
+from exact_tiled_attention_gb300 import attn_fwd, attn_fwd_fp8, gbattn_device_status, gbattn_timeline_set
 from exact_tiled_attention_gb300.inputs import make_prefill
 from tests.parity_util import assert_attn_close, host_f32
 
@@ -61,3 +61,25 @@ def test_timeline_capacity_too_small_writes_nothing():
     attn_fwd(q, k, v, causal=True)
     torch.cuda.synchronize()
     assert int(rec.abs().sum()) == 0
+
+
+def test_timeline_fp8_records_every_unit_once():
+    B, H, Hkv, Sq, Sk, d = 1, 4, 2, 600, 500, 128
+    g = torch.Generator(device="cpu").manual_seed(9)
+    q, k, v = (torch.randn(B, h, s, d, generator=g).clamp(-4, 4).to(torch.float8_e4m3fn).cuda()
+               for h, s in ((H, Sq), (Hkv, Sk), (Hkv, Sk)))
+    n_pairs = -(-Sq // 256)
+    grid = B * H * n_pairs
+    rec = torch.zeros(grid, 4, dtype=torch.int64, device="cuda")
+    try:
+        gbattn_timeline_set(rec)
+        o, _ = attn_fwd_fp8(q, k, v, causal=True)
+        torch.cuda.synchronize()
+    finally:
+        gbattn_timeline_set(None)
+    assert gbattn_device_status() == 0
+    r = rec.cpu().numpy().astype(np.uint64)
+    assert (r[:, 0] > 0).all() and (r[:, 1] >= r[:, 0]).all()
+    units = sorted((int(u >> np.uint64(32)), int(u & np.uint64(0xFFFFFFFF))) for u in r[:, 3])
+    assert units == [(bh, p) for bh in range(B * H) for p in range(n_pairs)]
+    assert torch.isfinite(o.float()).all()
