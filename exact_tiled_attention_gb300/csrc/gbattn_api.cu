@@ -251,7 +251,8 @@ int attn_fwd_pair(const void* q, const void* k, const void* v, void* o, float* l
   if (static_cast<long long>(B) * H > 0x7FFFFFFFLL || static_cast<long long>(B) * Hkv > 0x7FFFFFFFLL)
     return GBATTN_EBADSHAPE;
   int* status = nullptr;
-  int rc = current_device(&status);
+  int sms = 0;
+  int rc = current_device(&status, &sms);
   if (rc != GBATTN_OK) return rc;
   PrefillArgs a{};
   a.q = q;
@@ -270,6 +271,12 @@ int attn_fwd_pair(const void* q, const void* k, const void* v, void* o, float* l
   a.bf16 = dtype == GBATTN_BF16;
   a.stream = static_cast<cudaStream_t>(stream);
   a.status = status;
+  a.num_sms = sms;
+  {
+    std::lock_guard<std::mutex> lock(g_timeline_mutex);
+    a.timeline = g_timeline;
+    a.timeline_capacity = g_timeline_capacity;
+  }
   return launch_prefill_pair(a) == 0 ? GBATTN_OK : GBATTN_ELAUNCH;
 }
 

@@ -485,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (p.timeline != nullptr && threadIdx.x == 0) {
+    // Timeline record of this CTA: start and end (%globaltimer ns), SM, unit.
     unsigned long long* rec = p.timeline + 4 * static_cast<size_t>(blockIdx.x);
     rec[0] = t_start;
     rec[1] = global_timer_ns();

@@ -80,6 +80,8 @@ struct Params {
   int head_group;  // (batch, head) pairs per L2 scheduling group
   float scale_log2;
   int* status;
+  int wave;                       // CTAs resident at once (one per SM)
+  unsigned long long* timeline;   // optional per-CTA records, or null
 };
 
 struct __align__(8) Barriers {
@@ -109,7 +111,8 @@ __device__ __forceinline__ int item_of_v(int j, int n) { return j <= n - 2 ? 2 *
 template <bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                        const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+                        const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_o,
+                        const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -122,6 +125,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x % 32;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
+  unsigned long long t_start = 0;
+  if (p.timeline != nullptr && threadIdx.x == 0) t_start = global_timer_ns();
 
   // ---- work unit (one per cluster), in groups of p.head_group (batch, head)
   // pairs whose K/V stay resident in L2, heads fastest.
@@ -187,6 +192,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int cb = 0; cb < 2; ++cb)
             tma_load_3d(sQ + x * kTileBytes + cb * kBlockBytes, &tmap_q, &bars->q_full, cb * 64, x ? q0_l : q0_h,
                         b * p.H + h, once);
+        {  // this CTA's Q rows of the cluster unit one wave ahead into L2
+          const int ahead = unit + p.wave / 2;
+          if (ahead < static_cast<int>(gridDim.x >> 1)) {
+            const int ga = ahead / (p.head_group * p.n_quads);
+            const int heads_a = min(p.head_group, BH - ga * p.head_group);
+            const int ra = ahead - ga * p.head_group * p.n_quads;
+            const int bh_a = ga * p.head_group + ra % heads_a;
+            const int qa = (ra / heads_a) * 4 * kBM + static_cast<int>(rank) * kBM;
+            for (int x = 0; x < 2; ++x)
+              if (qa + 2 * x * kBM < p.Sq)
+                for (int cb = 0; cb < 2; ++cb) tma_prefetch_l2_3d(&tmap_q, cb * 64, qa + 2 * x * kBM, bh_a);
+          }
+        }
         int issued = 0;
         for (int it = 0; it < n_items; ++it) {
           const int st = it % kStages;
@@ -489,8 +507,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const bool row_ok = q_row < p.Sq;
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
-      uint16_t* orow =
-          reinterpret_cast<uint16_t*>(p.o) + ((static_cast<size_t>(b) * p.H + h) * p.Sq + (row_ok ? q_row : 0)) * kD;
+      // O_X is staged in Q_X (dead since the last QK_X completed), 128-byte
+      // rows with 16-byte chunk c at chunk c ^ (row % 8), and written by one
+      // TMA store per 64-column block (rows past Sq are not written).
+      uint8_t* o_row = sQ + x * kTileBytes + row * 128;
 #pragma unroll 1
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t w[32];
@@ -506,11 +526,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * inv, __uint_as_float(w[2 * i + 1]) * inv);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        uint8_t* blk = o_row + (c / 2) * kBlockBytes;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int k = 0; k < 4; ++k) {
+          const int ch = (c % 2) * 4 + k;
+          *reinterpret_cast<uint4*>(blk + ((ch ^ (row & 7)) << 4)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
         }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1 + x, kBM);
+      if (wq == 0 && lane == 0) {
+        for (int cb = 0; cb < 2; ++cb)
+          tma_store_3d(&tmap_o, sQ + x * kTileBytes + cb * kBlockBytes, cb * 64, q0x, b * p.H + h);
+        bulk_commit_group();
+        bulk_wait_group_read0();
       }
       if (row_ok && p.lse != nullptr) {
         const float lse = (l > 0.f) ? (r * lam + __log2f(l)) * 0.69314718055994531f : -INFINITY;
@@ -524,21 +554,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   cluster_sync_all();
   tc_fence_after();
+  if (p.timeline != nullptr && threadIdx.x == 0) {
+    // Timeline record of this CTA: start and end (%globaltimer ns), SM, unit.
+    unsigned long long* rec = p.timeline + 4 * static_cast<size_t>(blockIdx.x);
+    rec[0] = t_start;
+    rec[1] = global_timer_ns();
+    rec[2] = sm_id();
+    rec[3] = static_cast<unsigned long long>(bh) << 32 | static_cast<unsigned>(quad);
+  }
   if (warp == kMmaWarpH) tmem_dealloc_pair(tmem, 512);
   cluster_sync_all();
 }
 
 template <bool BF16>
 int launch_pair_t(const PrefillArgs& a) {
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!make_tmap_3d(&tq, a.q, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
+      !make_tmap_3d(&to, a.o, BF16, kD, a.Sq, static_cast<long long>(a.B) * a.H, kBM) ||
       !make_tmap_3d(&tk, a.k, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, 64) ||
       !make_tmap_3d(&tv, a.v, BF16, kD, a.Sk, static_cast<long long>(a.B) * a.Hkv, kBN))
     return -1;
   auto kern = prefill_pair_kernel<BF16>;
   static std::atomic<unsigned long long> attr_done{0};  // per instantiation
   if (!set_smem_limit_once(kern, kSmemBytes, attr_done)) return -1;
-  Params p;
+  Params p{};
   p.o = a.o;
   p.lse = a.lse;
   p.B = a.B;
@@ -558,9 +597,11 @@ int launch_pair_t(const PrefillArgs& a) {
   }
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
+  p.wave = a.num_sms;
   const long long grid = 2LL * a.B * a.H * p.n_quads;
   if (grid > 0x7FFFFFFFLL) return -1;
-  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, p);
+  p.timeline = (a.timeline != nullptr && a.timeline_capacity >= grid) ? a.timeline : nullptr;
+  kern<<<static_cast<unsigned>(grid), kThreads, kSmemBytes, a.stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -382,15 +382,19 @@ int gbattn_selftest_bounded_wait(int arrive, void *stream);
 int gbattn_device_status(void);
 
 /*
- * gbattn_timeline_set -- per-CTA timeline of attn_fwd and attn_fwd_fp8
- * launches (a profiling aid; the method has no counterpart).  While set,
- * every such launch whose grid has at most `capacity` CTAs writes, for CTA
- * i, four unsigned 64-bit values at records[4 i .. 4 i + 3]:
+ * gbattn_timeline_set -- per-CTA timeline of forward launches (attn_fwd,
+ * attn_fwd_pair, attn_fwd_fp8; a profiling aid, the method has no
+ * counterpart).  While set, every such launch whose grid has at most
+ * `capacity` CTAs writes, for CTA i, four unsigned 64-bit values at
+ * records[4 i .. 4 i + 3]:
  *   [0] start and [1] end of the CTA, in %globaltimer nanoseconds,
  *   [2] the SM it ran on,
- *   [3] its work unit, (b * H + h) << 32 | query pair (rows 256 p .. 256 p + 255).
- * A launch with more CTAs than `capacity` writes nothing.  The grid of a
- * launch has B * H * ceil(Sq / 256) CTAs.  records is a device pointer owned
+ *   [3] its work unit, (b * H + h) << 32 | u: for attn_fwd and attn_fwd_fp8
+ *       u is the query pair (rows 256 u .. 256 u + 255), one CTA each, grid
+ *       B * H * ceil(Sq / 256); for attn_fwd_pair u is the 512-row query
+ *       block of the CTA's cluster (CTAs 2 c and 2 c + 1), grid
+ *       2 * B * H * ceil(Sq / 512).
+ * A launch with more CTAs than `capacity` writes nothing.  records is a device pointer owned
  * by the caller, 8-byte aligned, at least 32 * capacity bytes, and must stay
  * valid until the launches that write it have completed.  records = NULL
  * turns the timeline off (capacity is then ignored).  The setting is
