@@ -163,7 +163,8 @@ template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
-                    const __grid_constant__ CUtensorMap tmap_do, const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmap_do, const __grid_constant__ CUtensorMap tmap_dk,
+                    const __grid_constant__ CUtensorMap tmap_dv, const BwdParams p) {
   using C = ColCfg<D>;
   using Bars = typename C::Bars;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -558,8 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     const float mul = wg ? p.scale : 1.f;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(wg ? p.dk : p.dv) +
-                    (static_cast<long long>(bkv) * p.Sk + key) * D;
+    // dV (warpgroup 0) / dK (warpgroup 1) staged in this CTA's own V / K
+    // tile (dead once every MMA has completed: acc_done), 128-byte rows with
+    // 16-byte chunk c at chunk c ^ (row % 8), and written by TMA (rows past
+    // Sk are not written).
+    uint8_t* stage = smem + (wg ? C::kOffK : C::kOffV) + kl * 128;
 #pragma unroll 1
     for (int c = 0; c < D / 32; ++c) {
       uint32_t w[32];
@@ -571,15 +575,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = 0u;
       }
-      if (key < p.Sk) {
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
+      uint8_t* blk = stage + (c / 2) * kBlock;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      for (int k = 0; k < 4; ++k) {
+        const int ch = (c % 2) * 4 + k;
+        *reinterpret_cast<uint4*>(blk + ((ch ^ (kl & 7)) << 4)) =
+            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
       }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + wg, 128);
+    if (warp % 4 == 0 && lane == 0) {
+      for (int cb = 0; cb < D / 64; ++cb)
+        tma_store_3d(wg ? &tmap_dk : &tmap_dv, smem + (wg ? C::kOffK : C::kOffV) + cb * kBlock, cb * 64, k0, bkv);
+      bulk_commit_group();
+      bulk_wait_group_read0();
     }
   }
 
@@ -623,7 +637,7 @@ struct RowCfg {
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
-                  const BwdParams p) {
+                  const __grid_constant__ CUtensorMap tmap_dq, const BwdParams p) {
   using C = RowCfg<D>;
   using Bars = typename C::Bars;
   extern __shared__ uint8_t smem_raw[];
@@ -886,7 +900,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       have = __all_sync(0xffffffffu, have);
       tc_fence_after();
     }
-    uint16_t* dst = reinterpret_cast<uint16_t*>(p.dq) + grow * D + wg * (D / 2);
+    // dQ staged in the first K slot of the ring (every load has been consumed
+    // and every MMA has completed: acc_done), 128-byte rows with 16-byte
+    // chunk c at chunk c ^ (row % 8), and written by TMA (rows past Sq are
+    // not written).
+    uint8_t* stage = smem + C::kOffKV + rl * 128;
 #pragma unroll 1
     for (int c = 0; c < D / 64; ++c) {
       uint32_t w[32];
@@ -898,15 +916,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = 0u;
       }
-      if (row_ok) {
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * p.scale, __uint_as_float(w[2 * i + 1]) * p.scale);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * p.scale, __uint_as_float(w[2 * i + 1]) * p.scale);
+      const int col = wg * (D / 2) + c * 32;  // first of these 32 columns
+      uint8_t* blk = stage + (col / 64) * kBlock;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      for (int k = 0; k < 4; ++k) {
+        const int ch = (col % 64) / 8 + k;
+        *reinterpret_cast<uint4*>(blk + ((ch ^ (rl & 7)) << 4)) =
+            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
       }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 256);
+    if (warp == 0 && lane == 0) {
+      for (int cb = 0; cb < D / 64; ++cb)
+        tma_store_3d(&tmap_dq, smem + C::kOffKV + cb * kBlock, cb * 64, q0, b * p.H + h);
+      bulk_commit_group();
+      bulk_wait_group_read0();
     }
   }
 
@@ -960,8 +989,11 @@ int head_group_for(long long per_head_bytes, long long heads) {
 
 template <int D, bool BF16, bool CAUSAL>
 int launch_bwd_t(const BackwardArgs& a) {
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!make_tmap_3d(&tq, a.q, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tdq, a.dq, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
+      !make_tmap_3d(&tdk, a.dk, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
+      !make_tmap_3d(&tdv, a.dv, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
       !make_tmap_3d(&tdo, a.dout, BF16, D, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
       !make_tmap_3d(&tk, a.k, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
       !make_tmap_3d(&tv, a.v, BF16, D, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
@@ -1003,13 +1035,13 @@ int launch_bwd_t(const BackwardArgs& a) {
   const long long grid_a = static_cast<long long>(a.B) * a.Hkv * p.n_ktiles;
   if (grid_a > 0x7FFFFFFFLL) return -1;
   bwd_dkdv_kernel<D, BF16, CAUSAL><<<static_cast<unsigned>(grid_a), kThreads, ColCfg<D>::kSmemBytes, a.stream>>>(
-      tq, tk, tv, tdo, p);
+      tq, tk, tv, tdo, tdk, tdv, p);
   // row owner: a query head re-reads its KV head's K and V
   BwdParams pr = p;
   pr.head_group = head_group_for(static_cast<long long>(a.Sk) * D * 4, static_cast<long long>(a.B) * a.H);
   const long long grid_b = static_cast<long long>(a.B) * a.H * p.n_qtiles;
   if (grid_b > 0x7FFFFFFFLL) return -1;
-  bwd_dq_kernel<D, BF16, CAUSAL><<<static_cast<unsigned>(grid_b), kThreads, RowCfg<D>::kSmemBytes, a.stream>>>(tk, tv, pr);
+  bwd_dq_kernel<D, BF16, CAUSAL><<<static_cast<unsigned>(grid_b), kThreads, RowCfg<D>::kSmemBytes, a.stream>>>(tk, tv, tdq, pr);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -134,6 +134,7 @@ template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_atomic_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
+                      const __grid_constant__ CUtensorMap tmap_dk, const __grid_constant__ CUtensorMap tmap_dv,
                       const AtomicParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {  // uniform over the CTA
@@ -518,7 +519,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     const float mul = wg ? p.scale : 1.f;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(wg ? p.dk : p.dv) + (static_cast<long long>(bkv) * p.Sk + key) * kD;
+    // dV (warpgroup 0) / dK (warpgroup 1) staged in this CTA's own V / K
+    // tile (dead once every MMA has completed: acc_done), 128-byte rows with
+    // 16-byte chunk c at chunk c ^ (row % 8), and written by TMA (rows past
+    // Sk are not written).  A thread storing its own 256-byte row to global
+    // memory instead touches one cache line per lane and store instruction.
+    uint8_t* stage = smem + (wg ? kOffK : kOffV) + kl * 128;
 #pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       uint32_t w[32];
@@ -530,15 +536,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = 0u;
       }
-      if (key < p.Sk) {
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
+      uint8_t* blk = stage + (c / 2) * kBlock;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      for (int k = 0; k < 4; ++k) {
+        const int ch = (c % 2) * 4 + k;
+        *reinterpret_cast<uint4*>(blk + ((ch ^ (kl & 7)) << 4)) =
+            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
       }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + wg, 128);
+    if (warp % 4 == 0 && lane == 0) {
+      for (int cb = 0; cb < kD / 64; ++cb)
+        tma_store_3d(wg ? &tmap_dk : &tmap_dv, smem + (wg ? kOffK : kOffV) + cb * kBlock, cb * 64, k0, bkv);
+      bulk_commit_group();
+      bulk_wait_group_read0();
     }
   }
 
@@ -599,7 +615,8 @@ template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_atomic64_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                         const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_do,
-                        const __grid_constant__ CUtensorMap tmap_dq, const AtomicParams p) {
+                        const __grid_constant__ CUtensorMap tmap_dq, const __grid_constant__ CUtensorMap tmap_dk,
+                        const __grid_constant__ CUtensorMap tmap_dv, const AtomicParams p) {
   // this kernel's layout (shadows the 128-dim constants)
   constexpr int kD = d64::kD, kTile = d64::kTile, kStages = d64::kStages;
   constexpr int kOffK = d64::kOffK, kOffV = d64::kOffV, kOffQ = d64::kOffQ, kOffDO = d64::kOffDO;
@@ -981,7 +998,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
     }
     const float mul = wg ? p.scale : 1.f;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(wg ? p.dk : p.dv) + (static_cast<long long>(bkv) * p.Sk + key) * kD;
+    // dV (warpgroup 0) / dK (warpgroup 1) staged in this CTA's own V / K
+    // tile (dead once every MMA has completed: acc_done), 128-byte rows with
+    // 16-byte chunk c at chunk c ^ (row % 8), and written by TMA (rows past
+    // Sk are not written).  A thread storing its own 256-byte row to global
+    // memory instead touches one cache line per lane and store instruction.
+    uint8_t* stage = smem + (wg ? kOffK : kOffV) + kl * 128;
 #pragma unroll 1
     for (int c = 0; c < kD / 32; ++c) {
       uint32_t w[32];
@@ -993,15 +1015,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) w[i] = 0u;
       }
-      if (key < p.Sk) {
-        uint32_t pk[16];
+      uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack2<BF16>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
+      uint8_t* blk = stage + (c / 2) * kBlock;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      for (int k = 0; k < 4; ++k) {
+        const int ch = (c % 2) * 4 + k;
+        *reinterpret_cast<uint4*>(blk + ((ch ^ (kl & 7)) << 4)) =
+            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
       }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1 + wg, 128);
+    if (warp % 4 == 0 && lane == 0) {
+      for (int cb = 0; cb < kD / 64; ++cb)
+        tma_store_3d(wg ? &tmap_dk : &tmap_dv, smem + (wg ? kOffK : kOffV) + cb * kBlock, cb * 64, k0, bkv);
+      bulk_commit_group();
+      bulk_wait_group_read0();
     }
   }
 
@@ -1077,11 +1109,13 @@ int head_group_atomic(long long per_head_bytes, long long heads) {
 
 template <int DH, bool BF16, bool CAUSAL>
 int launch_atomic_t(const BackwardArgs& a) {
-  CUtensorMap tq, tk, tv, tdo, tdq;
+  CUtensorMap tq, tk, tv, tdo, tdq, tdk, tdv;
   if (!make_tmap_3d(&tq, a.q, BF16, DH, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
       !make_tmap_3d(&tdo, a.dout, BF16, DH, a.Sq, static_cast<long long>(a.B) * a.H, kT) ||
       !make_tmap_3d(&tk, a.k, BF16, DH, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
-      !make_tmap_3d(&tv, a.v, BF16, DH, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
+      !make_tmap_3d(&tv, a.v, BF16, DH, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
+      !make_tmap_3d(&tdk, a.dk, BF16, DH, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT) ||
+      !make_tmap_3d(&tdv, a.dv, BF16, DH, a.Sk, static_cast<long long>(a.B) * a.Hkv, kT))
     return -1;
   if (DH == 64 && !make_tmap_3d_f32(&tdq, a.dq_acc, DH, a.Sq, static_cast<long long>(a.B) * a.H, 32, 32))
     return -1;
@@ -1120,9 +1154,10 @@ int launch_atomic_t(const BackwardArgs& a) {
   if (grid > 0x7FFFFFFFLL) return -1;
   if constexpr (DH == 64)
     bwd_atomic64_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid), kThreads, smem_bytes, a.stream>>>(tq, tk, tv, tdo,
-                                                                                                      tdq, p);
+                                                                                                      tdq, tdk, tdv, p);
   else
-    bwd_atomic_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid), kThreads, smem_bytes, a.stream>>>(tq, tk, tv, tdo, p);
+    bwd_atomic_kernel<BF16, CAUSAL><<<static_cast<unsigned>(grid), kThreads, smem_bytes, a.stream>>>(tq, tk, tv, tdo,
+                                                                                                    tdk, tdv, p);
   {
     const long long n8 = n_rows * (DH / 8);
     const long long blocks = (n8 + 255) / 256;
