@@ -333,30 +333,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      const int k0 = j * kBN;
+      const bool masked = (k0 + kBN > p.Sk) || (CAUSAL && (k0 + kBN - 1 > q0x + p.delta));
+      // S row -> registers; an unmasked tile's loads also return each
+      // 32-column block's maximum (tcgen05.ld.red)
       uint32_t u[kBN];
+      float mq[kBN / 32];
+      if (masked) {
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+        for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld32_max(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]), mq[c]);
+      }
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
       tc_fence_before();
       mbar_arrive(&bars->s_free[x]);
       float* s = reinterpret_cast<float*>(u);
-      const int k0 = j * kBN;
-      if ((k0 + kBN > p.Sk) || (CAUSAL && (k0 + kBN - 1 > q0x + p.delta))) {
+      float mx;
+      if (masked) {
         const int lim = CAUSAL ? min(p.Sk - 1, q_row + p.delta) : p.Sk - 1;  // last visible key
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
           if (k0 + c > lim) s[c] = -INFINITY;
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i < kBN ? c + 8 + i : c + i]);
+        mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      } else {
+        mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       }
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < kBN; c += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i < kBN ? c + 8 + i : c + i]);
-      const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       float gamma = 1.f;
       if (j == 0) {
         r = mx;

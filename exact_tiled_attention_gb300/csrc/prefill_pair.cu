@@ -384,11 +384,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // ---- S row -> registers, then S_X of this CTA is free
+      // ---- S row -> registers, then S_X of this CTA is free; a tile without
+      // a key tail also gets each 32-column block's maximum from the loads
+      const int k0 = j * kBN;
+      const bool key_tail = k0 + kBN > p.Sk;
       uint32_t u[kBN];
+      float mq[kBN / 32];
+      if (key_tail) {
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld32(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld32_max(s_tmem + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]), mq[c]);
+      }
       tmem_wait_ld();
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
@@ -399,22 +409,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         else mbar_arrive_cluster_smem_release(s_free_addr);
       }
       float* s = reinterpret_cast<float*>(u);
-      const int k0 = j * kBN;
-      if (k0 + kBN > p.Sk) {  // key tail
+      float mx;
+      if (key_tail) {
 #pragma unroll
         for (int c = 0; c < kBN; ++c)
           if (k0 + c >= p.Sk) s[c] = -INFINITY;
+        // ---- row maximum: eight independent three-input max chains
+        float mx8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < kBN; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i < kBN ? c + 8 + i : c + i]);
+        mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      } else {
+        mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       }
-      // ---- row maximum: eight independent three-input max chains
-      float mx8[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < kBN; c += 16)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = fmax3(mx8[i], s[c + i], s[c + 8 + i < kBN ? c + 8 + i : c + i]);
-      const float mx =
-          fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
       float gamma = 1.f;
       if (j == 0) {
         r = mx;
