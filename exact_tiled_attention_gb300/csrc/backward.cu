@@ -473,17 +473,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // column c with c0 + c + delta < key.
       const bool need_mask = (k0 + kT > p.Sk) || (CAUSAL && (k0 + kT - 1 > c0 + p.delta));
       const int first_c = (key >= p.Sk) ? 64 : (CAUSAL ? key - p.delta - c0 : 0);
+      const float2 lam2 = make_float2(lam, lam);
+      if (!need_mask) {  // block-uniform: every block but the diagonal and ragged ones
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = st_l[c4];  // broadcast read
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = st_l[c4];  // broadcast read
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = 4 * c4 + 2 * i;
-          const float2 e = ex2_pair(make_float2(fmaf(x[c], lam, -(i ? l4.z : l4.x)),
-                                                fmaf(x[c + 1], lam, -(i ? l4.w : l4.y))),
-                                    c / 2);
-          x[c] = (need_mask && c < first_c) ? 0.f : e.x;
-          x[c + 1] = (need_mask && c + 1 < first_c) ? 0.f : e.y;
+          for (int i = 0; i < 2; ++i) {
+            const int c = 4 * c4 + 2 * i;
+            const float2 nl = i ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 e = ex2_pair(ffma2(make_float2(x[c], x[c + 1]), lam2, nl), c / 2);
+            x[c] = e.x;
+            x[c + 1] = e.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = st_l[c4];  // broadcast read
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = 4 * c4 + 2 * i;
+            const float2 nl = i ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 e = ex2_pair(ffma2(make_float2(x[c], x[c + 1]), lam2, nl), c / 2);
+            x[c] = (c < first_c) ? 0.f : e.x;
+            x[c + 1] = (c + 1 < first_c) ? 0.f : e.y;
+          }
         }
       }
       if constexpr (C::kPTSmem) {
@@ -538,10 +553,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = st_d[hf * 8 + c4];  // broadcast read
           const int cb = hf * 32 + 4 * c4;
-          x[cb + 0] *= __uint_as_float(w[4 * c4 + 0]) - d4.x;
-          x[cb + 1] *= __uint_as_float(w[4 * c4 + 1]) - d4.y;
-          x[cb + 2] *= __uint_as_float(w[4 * c4 + 2]) - d4.z;
-          x[cb + 3] *= __uint_as_float(w[4 * c4 + 3]) - d4.w;
+          const float2 a = fmul2(make_float2(x[cb], x[cb + 1]),
+                                 fadd2(make_float2(__uint_as_float(w[4 * c4]), __uint_as_float(w[4 * c4 + 1])),
+                                       make_float2(-d4.x, -d4.y)));
+          const float2 b2 = fmul2(make_float2(x[cb + 2], x[cb + 3]),
+                                  fadd2(make_float2(__uint_as_float(w[4 * c4 + 2]), __uint_as_float(w[4 * c4 + 3])),
+                                        make_float2(-d4.z, -d4.w)));
+          x[cb] = a.x;
+          x[cb + 1] = a.y;
+          x[cb + 2] = b2.x;
+          x[cb + 3] = b2.y;
         }
         uint32_t pk[16];
         pack32<BF16>(x, hf * 32, pk);
@@ -847,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool need_mask = last_c < 63;
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float2 e = ex2_pair(make_float2(fmaf(x[c], lam, -l2), fmaf(x[c + 1], lam, -l2)), c / 2);
+        const float2 e = ex2_pair(ffma2(make_float2(x[c], x[c + 1]), make_float2(lam, lam), make_float2(-l2, -l2)), c / 2);
         x[c] = (need_mask && c > last_c) ? 0.f : e.x;
         x[c + 1] = (need_mask && c + 1 > last_c) ? 0.f : e.y;
       }
@@ -868,7 +889,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&bars->dp_free);  // dP(j+1) may now overwrite the columns
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[hf * 32 + i] *= __uint_as_float(w[i]) - Dr;
+        for (int i = 0; i < 32; i += 2) {
+          const float2 v = fmul2(make_float2(x[hf * 32 + i], x[hf * 32 + i + 1]),
+                                 fadd2(make_float2(__uint_as_float(w[i]), __uint_as_float(w[i + 1])), make_float2(-Dr, -Dr)));
+          x[hf * 32 + i] = v.x;
+          x[hf * 32 + i + 1] = v.y;
+        }
       }
       // dS row into shared memory (column block wg, row rl; 16-byte chunk c
       // at chunk c ^ (rl % 8)) once the dQ product of tile j-1 has read it.

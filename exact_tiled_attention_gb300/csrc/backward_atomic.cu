@@ -436,17 +436,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       // column c with c0 + c + delta < key.
       const bool need_mask = (k0 + kT > p.Sk) || (CAUSAL && (k0 + kT - 1 > c0 + p.delta));
       const int first_c = (key >= p.Sk) ? 64 : (CAUSAL ? key - p.delta - c0 : 0);
+      const float2 lam2 = make_float2(lam, lam);
+      if (!need_mask) {  // block-uniform: every block but the diagonal and ragged ones
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = st_l[c4];  // broadcast read
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = st_l[c4];  // broadcast read
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = 4 * c4 + 2 * i;
-          const float2 e = ex2_pair(make_float2(fmaf(x[c], lam, -(i ? l4.z : l4.x)),
-                                                fmaf(x[c + 1], lam, -(i ? l4.w : l4.y))),
-                                    c / 2);
-          x[c] = (need_mask && c < first_c) ? 0.f : e.x;
-          x[c + 1] = (need_mask && c + 1 < first_c) ? 0.f : e.y;
+          for (int i = 0; i < 2; ++i) {
+            const int c = 4 * c4 + 2 * i;
+            const float2 nl = i ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 e = ex2_pair(ffma2(make_float2(x[c], x[c + 1]), lam2, nl), c / 2);
+            x[c] = e.x;
+            x[c + 1] = e.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = st_l[c4];  // broadcast read
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = 4 * c4 + 2 * i;
+            const float2 nl = i ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 e = ex2_pair(ffma2(make_float2(x[c], x[c + 1]), lam2, nl), c / 2);
+            x[c] = (c < first_c) ? 0.f : e.x;
+            x[c + 1] = (c + 1 < first_c) ? 0.f : e.y;
+          }
         }
       }
       {
@@ -487,10 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = st_d[hf * 8 + c4];  // broadcast read
           const int cb = hf * 32 + 4 * c4;
-          pk[2 * c4] = pack2<BF16>(x[cb] * (__uint_as_float(w[4 * c4]) - d4.x),
-                                   x[cb + 1] * (__uint_as_float(w[4 * c4 + 1]) - d4.y));
-          pk[2 * c4 + 1] = pack2<BF16>(x[cb + 2] * (__uint_as_float(w[4 * c4 + 2]) - d4.z),
-                                       x[cb + 3] * (__uint_as_float(w[4 * c4 + 3]) - d4.w));
+          const float2 a = fmul2(make_float2(x[cb], x[cb + 1]),
+                                 fadd2(make_float2(__uint_as_float(w[4 * c4]), __uint_as_float(w[4 * c4 + 1])),
+                                       make_float2(-d4.x, -d4.y)));
+          const float2 b2 = fmul2(make_float2(x[cb + 2], x[cb + 3]),
+                                  fadd2(make_float2(__uint_as_float(w[4 * c4 + 2]), __uint_as_float(w[4 * c4 + 3])),
+                                        make_float2(-d4.z, -d4.w)));
+          pk[2 * c4] = pack2<BF16>(a.x, a.y);
+          pk[2 * c4 + 1] = pack2<BF16>(b2.x, b2.y);
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -965,10 +984,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 d4 = st_d[hf * 8 + c4];
           const int cb = hf * 32 + 4 * c4;
-          pk[2 * c4] = pack2<BF16>(x[cb] * (__uint_as_float(w[4 * c4]) - d4.x),
-                                   x[cb + 1] * (__uint_as_float(w[4 * c4 + 1]) - d4.y));
-          pk[2 * c4 + 1] = pack2<BF16>(x[cb + 2] * (__uint_as_float(w[4 * c4 + 2]) - d4.z),
-                                       x[cb + 3] * (__uint_as_float(w[4 * c4 + 3]) - d4.w));
+          const float2 a = fmul2(make_float2(x[cb], x[cb + 1]),
+                                 fadd2(make_float2(__uint_as_float(w[4 * c4]), __uint_as_float(w[4 * c4 + 1])),
+                                       make_float2(-d4.x, -d4.y)));
+          const float2 b2 = fmul2(make_float2(x[cb + 2], x[cb + 3]),
+                                  fadd2(make_float2(__uint_as_float(w[4 * c4 + 2]), __uint_as_float(w[4 * c4 + 3])),
+                                        make_float2(-d4.z, -d4.w)));
+          pk[2 * c4] = pack2<BF16>(a.x, a.y);
+          pk[2 * c4 + 1] = pack2<BF16>(b2.x, b2.y);
         }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {

@@ -481,6 +481,17 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   return r;
 }
 
+// Packed two-lane fp32 multiply.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "mul.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
 // Packed two-lane fp32 add.
 __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
   float2 r;
