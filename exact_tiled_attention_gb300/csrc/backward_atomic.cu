@@ -937,17 +937,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4* st_l = reinterpret_cast<const float4*>(stats + s * 2 * kT + wg * 64);
       const bool need_mask = (k0 + kT > p.Sk) || (CAUSAL && (k0 + kT - 1 > c0 + p.delta));
       const int first_c = (key >= p.Sk) ? 64 : (CAUSAL ? key - p.delta - c0 : 0);
+      const float2 lam2 = make_float2(lam, lam);
+      if (!need_mask) {  // block-uniform: every block but the diagonal and ragged ones
 #pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 l4 = st_l[c4];
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = st_l[c4];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int c = 4 * c4 + 2 * i;
-          const float2 e = ex2_pair(make_float2(fmaf(x[c], lam, -(i ? l4.z : l4.x)),
-                                                fmaf(x[c + 1], lam, -(i ? l4.w : l4.y))),
-                                    c / 2);
-          x[c] = (need_mask && c < first_c) ? 0.f : e.x;
-          x[c + 1] = (need_mask && c + 1 < first_c) ? 0.f : e.y;
+          for (int i = 0; i < 2; ++i) {
+            const int c = 4 * c4 + 2 * i;
+            const float2 nl = i ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 e = ex2_pair(ffma2(make_float2(x[c], x[c + 1]), lam2, nl), c / 2);
+            x[c] = e.x;
+            x[c + 1] = e.y;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < 16; ++c4) {
+          const float4 l4 = st_l[c4];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = 4 * c4 + 2 * i;
+            const float2 nl = i ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+            const float2 e = ex2_pair(ffma2(make_float2(x[c], x[c + 1]), lam2, nl), c / 2);
+            x[c] = (c < first_c) ? 0.f : e.x;
+            x[c + 1] = (c + 1 < first_c) ? 0.f : e.y;
+          }
         }
       }
       {
