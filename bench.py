@@ -120,10 +120,16 @@ def decode_algorithmic_bytes(w, lens) -> int:
 
 
 def kernel_source_hash(files) -> str:
+    """Hash of the kernel sources with comments and runs of white space
+    removed: an edit to a comment leaves the committed DRAM figures valid,
+    any change to the code itself invalidates them."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

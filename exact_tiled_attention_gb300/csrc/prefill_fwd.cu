@@ -24,12 +24,12 @@
 // copied S_X(j) into registers.  At d = 128 tensor memory is full (S and O
 // of both tiles), so P goes to shared memory and P.V reads both operands
 // from there (8 KB per 16-key step for 16 KB of tensor work: balanced).  At
-// d = 64 the P.V product has N = 64, so a shared-memory A operand would be
-// re-read for half the columns and the MMA would wait on shared-memory
-// bandwidth (measured: ~90 cycles per 16-key step, and the issuing thread
-// blocks behind it); the 128 columns S and O leave free hold P for both
-// tiles, and P.V reads A from tensor memory (a TS MMA) and only V from
-// shared memory.
+// d = 64 the 128 columns S and O leave free hold P for both tiles: the
+// softmax writes P with tcgen05.st and P.V reads A from tensor memory (a TS
+// MMA) and only V from shared memory.  Measured against P in shared memory
+// at d = 64: 0.0575 -> 0.0498 ms.  The tensor pipe takes about as long for
+// either form (48 and 45 cycles per 128x64x16 step); the shared-memory form
+// adds the P stores, a proxy fence and 4 KB more operand reads per step.
 //
 // Warp roles (384 threads = three warpgroups):
 //   warps 0-3   softmax + correction + epilogue of tile H (thread = one row)
@@ -49,6 +49,11 @@
 //              [PV_X(j-1) done] rescale O if needed, write P_X(j) -> signal
 // K/V slots are loaded in the order the MMAs need them:
 //   K_0, K_1, V_0, K_2, V_1, ..., K_{n-1}, V_{n-2}, V_{n-1}.
+// Stagger: QK_L(0) waits until the softmax of tile H has copied S_H(0) into
+// registers, so the two tiles' softmax chains run a few hundred cycles apart
+// instead of in lockstep (their exponentials, tensor-memory loads and P
+// stores then contend less for the same units; measured 1.4-3.6 % faster at
+// d = 128, no change at d = 64).
 //
 // Online softmax (M4.3 0x07-0x09; M4.6 0x09 conditional rescaling): each
 // softmax thread keeps its row's retained reference r (raw score units) and
@@ -124,6 +129,7 @@ struct __align__(8) Barriers {
   uint64_t p_free[2];     // P.V complete
   uint64_t o_full[2];
   uint64_t mma_done[2];
+  uint64_t stagger;  // tile H has read its first S: tile L may start
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -266,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_full[x], 1);
       mbar_init(&bars->mma_done[x], 1);
     }
+    mbar_init(&bars->stagger, kBM);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -354,6 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         };
         bool ok = nt == 0 || bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma);
+        // Tile L's first QK waits until tile H has read S_H(0), so the two
+        // tiles' softmax chains run staggered instead of in lockstep.
+        if (ok && x == 1 && nt_h > 0 && nt_l > 0)
+          ok = bounded_wait(&bars->stagger, 0, abort_flag, p.status, kStatusTimeoutMma);
         // S_X(0)
         if (ok && nt > 0) {
           uint32_t par;
@@ -465,6 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kBN / 32; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&u[c * 32]));
       tc_fence_before();
       mbar_arrive(&bars->s_free[x]);
+      if (x == 0 && j == 0 && nt_l > 0) mbar_arrive(&bars->stagger);
       float* s = reinterpret_cast<float*>(u);
       float mx;
       if (tail || diag) {

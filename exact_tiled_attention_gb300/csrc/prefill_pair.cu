@@ -33,6 +33,9 @@
 //   P written  each softmax warp arrives once on rank 0's p_full (4 + 4)
 //   P.V done   multicast commits to pblk_free (per P block slot) / o_full
 //   slot free  multicast commits to kv_empty of both CTAs
+//   stagger    tile H's softmax warps of both CTAs arrive once, after their
+//              first S copy, on rank 0's stagger; tile L's issuer waits for
+//              it before QK_L(0), so the tiles' softmax chains run apart
 // Tensor memory is allocated and freed pair-collectively (warp 8 of each
 // CTA); the kernel ends with two cluster barriers around the free.
 //
@@ -96,6 +99,7 @@ struct __align__(8) Barriers {
   uint64_t pblk_free[2][kPSlots];  // the P.V half reading this P block slot is complete
   uint64_t o_full[2];
   uint64_t mma_done[2];
+  uint64_t stagger;  // rank 0: tile H of both CTAs has read its first S
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -162,6 +166,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&bars->o_full[x], 1);
       mbar_init(&bars->mma_done[x], 1);
     }
+    mbar_init(&bars->stagger, 8);  // one arrival per tile-H softmax warp of either CTA
     bars->abort_flag = 0;
     fence_mbar_init();
   }
@@ -309,6 +314,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         };
         bool ok = bounded_wait(&bars->q_full, 0, abort_flag, p.status, kStatusTimeoutMma) &&
                   bounded_wait_cluster(&bars->q_peer, 0, abort_flag, p.status, kStatusTimeoutMma);
+        // Tile L's first QK waits until tile H has read S_H(0) in both CTAs, so
+        // the two tiles' softmax chains run staggered instead of in lockstep.
+        if (ok && x == 1) ok = bounded_wait_cluster(&bars->stagger, 0, abort_flag, p.status, kStatusTimeoutMma);
         if (ok) {
           const int st = wait_item(item_of_k(0));
           ok = st >= 0;
@@ -369,6 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Rank 0's s_free / p_full (local address on rank 0, remote on rank 1).
     const uint32_t s_free_addr = mapa_shared(&bars->s_free[x], 0);
     const uint32_t p_full_addr = mapa_shared(&bars->p_full[x], 0);
+    const uint32_t stagger_addr = mapa_shared(&bars->stagger, 0);
     // This row of P_X in shared memory: block slots of 64 keys in 128-byte
     // rows; 16-byte chunk c of the row sits at chunk c ^ (row % 8).
     uint8_t* p_row = sP + x * kPSlots * kBlockBytes + row * 128;
@@ -407,6 +416,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {  // rank 0: local arrive; rank 1: shared-memory release + relaxed remote arrive
         if (leader) mbar_arrive(&bars->s_free[x]);
         else mbar_arrive_cluster_smem_release(s_free_addr);
+        if (x == 0 && j == 0) {
+          if (leader) mbar_arrive(&bars->stagger);
+          else mbar_arrive_cluster_smem_release(stagger_addr);
+        }
       }
       float* s = reinterpret_cast<float*>(u);
       float mx;

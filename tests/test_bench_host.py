@@ -1,6 +1,6 @@
 """The bench's host-side bookkeeping (no GPU): batch overrides rename the
 workload, and DRAM traffic from a committed ncu record is reported only for
-the workload and kernel source it was taken on."""
+the workload and kernel code it was taken on (comments aside)."""
 import json
 import os
 
@@ -30,7 +30,10 @@ def test_traffic_record_needs_matching_workload_and_source(tmp_path, monkeypatch
     assert bench.ncu_traffic(key, sources, "causal_bf16_b4_h16_s8192_d128") == 123
     assert bench.ncu_traffic(key, sources, "causal_bf16_b1_h16_s8192_d128") is None  # another batch
     assert bench.ncu_traffic("other", sources, "causal_bf16_b4_h16_s8192_d128") is None
-    src.write_bytes(src.read_bytes() + b"\n// changed\n")
+    original = src.read_bytes()
+    src.write_bytes(original + b"\n// a comment\n/* and a block\n comment */\n")
+    assert bench.ncu_traffic(key, sources, "causal_bf16_b4_h16_s8192_d128") == 123  # comments only
+    src.write_bytes(original + b"\nstatic int changed = 1;\n")
     assert bench.ncu_traffic(key, sources, "causal_bf16_b4_h16_s8192_d128") is None  # stale source
 
 
