@@ -88,7 +88,7 @@ struct __align__(8) Bars {
   uint64_t qd_empty[kStages];
   uint64_t s_full, dp_full;
   uint64_t p_full, ds_full;
-  uint64_t dv_done, dk_done;
+  uint64_t dv_done;
   uint64_t dq_full, dq_free;
   uint64_t acc_done;
   uint32_t tmem_base;
@@ -180,7 +180,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->p_full, 256);
     mbar_init(&bars->ds_full, 256);
     mbar_init(&bars->dv_done, 1);
-    mbar_init(&bars->dk_done, 1);
     mbar_init(&bars->dq_full, 1);
     mbar_init(&bars->dq_free, 128);
     mbar_init(&bars->acc_done, 2);
@@ -382,7 +381,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_f16_ss(tmem + kColDK, ds_kmaj + kstep_kmajor(kk), bd + kstep_mnmajor(kk), kIdAcc,
                            (t > 0 || kk > 0) ? 1u : 0u);
             }
-            mma_commit(&bars->dk_done);
+            // (no commit for dK alone: dp_full of the next block, committed after
+            // dP^T(t+1), which this thread issues after dK(t), also covers dK(t))
             mma_commit(&bars->qd_empty[s]);
             // dP^T(t+1) over dQ^T(t) once the compute warpgroups drained it
             if (t + 1 < T) {
@@ -480,11 +480,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     // dP^T(t) -> dS^T(t) = P (dP - D), into shared memory once dQ^T(t-1) and
-    // dK(t-1) have read the previous one; 32 query columns at a time.
+    // dK(t-1) have read the previous one -- both are implied by dp_full(t):
+    // the dP^T/dS^T chain's thread issues dQ^T(t-1) and dK(t-1) before
+    // dP^T(t), and a commit covers every earlier MMA of its thread (one wait
+    // fewer per block: 1.6 % causal, 2.1 % GQA); 32 query columns at a time.
     auto phase_ds = [&](int t) -> bool {
       const int s = t % kStages;
-      bool ok = wait_bar(&bars->dp_full, t & 1, abort_flag, p.status);
-      if (t > 0) ok = ok && wait_bar(&bars->dk_done, (t - 1) & 1, abort_flag, p.status);
+      const bool ok = wait_bar(&bars->dp_full, t & 1, abort_flag, p.status);
       if (!__all_sync(0xffffffffu, ok)) return false;
       tc_fence_after();
       const float4* st_d = reinterpret_cast<const float4*>(stats + s * 2 * kT + kT + wg * 64);

@@ -19,10 +19,9 @@
 //   - one thread issues the MMAs of both SMs (half the issue work per SM);
 //   - the freed shared memory holds three 64-key P blocks per query tile
 //     instead of two: P(j) block b goes to block slot (2j + b) mod 3, so
-//     block 0 of P(j+1) never waits for P.V(j) and block 1 waits only for the
-//     first half of P.V(j).  The pair's handshakes cross the cluster (about
-//     570 cycles one way, measured), which a P buffer released in two halves
-//     would put on every tile's softmax chain.
+//     P(j+1) waits only for the first half of P.V(j) (one wait per key tile,
+//     before its first block), never for the whole of it.  The pair's
+//     handshakes cross the cluster (about 570 cycles one way, measured).
 //
 // Cross-CTA protocol (cluster-scope mbarriers; every wait bounded):
 //   loads      each CTA's TMA lane loads its Q tiles and K/V halves and
@@ -451,8 +450,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       l *= gamma;
       // ---- P = 2^(lambda*s - lambda*r), row sum, pack to 16 bits, store the
-      // row of P_X(j): block b (n = 2j + b) into slot n mod 3 once the P.V half
-      // that read the slot's previous block (n - 3) is complete; before the
+      // row of P_X(j): block b (n = 2j + b) into slot n mod 3 once the P.V
+      // halves that read the slots' previous blocks are complete; before the
       // last block, O is corrected once P.V_X(j-1) is complete.
       const float rs = (r == -INFINITY) ? 0.f : r * lam;
       const float2 lam2 = make_float2(lam, lam);
@@ -472,9 +471,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pk[c8 * 4 + i] = pack2<BF16>(t.x, t.y);
           }
         }
-        const int n = 2 * j + blk;
-        if (n >= kPSlots) {
-          ok = bounded_wait_cluster(&bars->pblk_free[x][n % kPSlots], ((n / kPSlots) - 1) & 1, abort_flag,
+        if (blk == 0 && j >= 1) {
+          // One wait per key tile: the first half of P.V_X(j-1) (block
+          // n' = 2j - 2) complete implies every earlier P.V of the issuer
+          // complete, so both slots P_X(j) goes to are free (block 0's slot
+          // was last read by the second half of P.V_X(j-2), block 1's by the
+          // first half of P.V_X(j-1)).  Measured 2.3 % faster than a wait
+          // per block.
+          const int np = 2 * j - 2;
+          ok = bounded_wait_cluster(&bars->pblk_free[x][np % kPSlots], (np / kPSlots) & 1, abort_flag,
                                     p.status, kStatusTimeoutSoftmax);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
