@@ -24,14 +24,18 @@
 // (the "standalone global transpose" design of that section's table).
 //
 // Tiles are 128 rows x 128 bytes (one 128-byte swizzle block): Q_H, Q_L,
-// P_H, P_L and an 8-slot ring of K / V^T tiles, 16 KiB each.  One MMA
-// instruction is 128 x 128 x 32.
+// two P buffers per query tile and an 8-slot ring of K / V^T tiles, 16 KiB
+// each.  One MMA instruction is 128 x 128 x 32.
 //
 // As in the 16-bit forward, tile L's first QK waits until tile H's softmax
-// has copied S_H(0) into registers (the two softmax chains run staggered),
-// and the softmax waits once per key tile for the whole of P.V(j-1) before
-// it overwrites P (measured: 0.677 -> 0.619 ms on the causal [4,16,8192,128]
-// workload against P released in two halves and a lockstep start).
+// has copied S_H(0) into registers (the two softmax chains run staggered).
+// P(j) goes to buffer j mod 2, last read by P.V(j-2); the issuer issues
+// QK(j) after P.V(j-2), and a commit covers every earlier MMA of its
+// thread, so S(j) ready implies that buffer free and the softmax has no P
+// wait of its own (only a correction of O waits for P.V(j-1)).  Measured on
+// the causal [4,16,8192,128] workload: 0.677 ms with P released in two
+// halves and a lockstep start, 0.619 ms with one release per key tile and
+// the stagger, 0.604 ms with the second buffer.
 #include <cuda_runtime.h>
 
 #include "gbattn_internal.h"
@@ -57,7 +61,7 @@ constexpr int kTile = kBM * 128;  // 16 KiB
 constexpr int kStages = 8;        // K / V^T ring slots
 constexpr int kQOff = 0;
 constexpr int kPOff = 2 * kTile;
-constexpr int kRingOff = 4 * kTile;
+constexpr int kRingOff = 6 * kTile;  // Q_H, Q_L, P_H[2], P_L[2]
 constexpr int kBarOff = kRingOff + kStages * kTile;
 constexpr int kSmemBytes = 1024 + kBarOff + 512;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s_col = tmem + x * kBN;
         const uint32_t o_col = tmem + 2 * kBN + x * kD;
         const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ + x * kTile), 16, 1024);
-        const uint64_t p_desc = smem_desc_sw128(smem_u32(sP + x * kTile), 16, 1024);
+        const uint64_t p_desc0 = smem_desc_sw128(smem_u32(sP + 2 * x * kTile), 16, 1024);
         auto slot_of = [&](int item, uint32_t& parity) {
           parity = (item / kStages) & 1;
           return item % kStages;
@@ -254,8 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kD / 32; ++kk) mma_f8_ss(s_col, q_desc + kk * 2, kd + kk * 2, kIdesc, kk > 0 ? 1u : 0u);
         };
-        auto issue_pv_steps = [&](int st, int kk0, int kk1, bool accumulate) {
+        auto issue_pv_steps = [&](int st, int kk0, int kk1, bool accumulate, int pbuf) {
           const uint64_t vd = smem_desc_sw128(ring_addr + st * kTile, 16, 1024);
+          const uint64_t p_desc = p_desc0 + ((pbuf * kTile) >> 4);
 #pragma unroll
           for (int kk = kk0; kk < kk1; ++kk)
             mma_f8_ss(o_col, p_desc + kk * 2, vd + kk * 2, kIdesc, (accumulate || kk > 0) ? 1u : 0u);
@@ -291,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = bounded_wait(&bars->kv_full[st], par, abort_flag, p.status, kStatusTimeoutMma))) break;
             if (!(ok = bounded_wait(&bars->p_full[x], j & 1, abort_flag, p.status, kStatusTimeoutMma))) break;
             tc_fence_after();
-            issue_pv_steps(st, 0, 4, j > 0);
+            issue_pv_steps(st, 0, 4, j > 0, j & 1);
             mma_commit(&bars->p_free[x]);
             if (j == nt - 1) mma_commit(&bars->o_full[x]);
             mma_commit(&bars->kv_empty[st]);
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t s_tmem = tmem + lane_off + x * kBN;
     const uint32_t o_tmem = tmem + lane_off + 2 * kBN + x * kD;
-    uint8_t* p_row = sP + x * kTile + row * 128;
+    uint8_t* p_row0 = sP + 2 * x * kTile + row * 128;  // buffer b at + b * kTile
     const float dqk = (p.dq ? p.dq[bkv] : 1.f) * (p.dk ? p.dk[bkv] : 1.f);
     const float dvs = p.dv ? p.dv[bkv] : 1.f;
     const float lam = p.scale * dqk * kLog2e;  // log2 units per raw Q8.K8 score
@@ -409,15 +414,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           sum4[1] = fadd2(sum4[1], te);
           pk[w] = pack4_e4m3(ta.x, ta.y, te.x, te.y);
         }
-        if (j > 0 && half == 0) {
-          // P.V(j-1) complete: P may be overwritten and O_X is stable
+        // P buffer j & 1 was last read by P.V(j-2), complete since s_full(j):
+        // the issuer issues QK(j) after P.V(j-2).  Only a correction of O
+        // waits for P.V(j-1).
+        if (j > 0 && half == 0 && __any_sync(0xffffffffu, gamma != 1.f)) {
           ok = bounded_wait(&bars->p_free[x], (j - 1) & 1, abort_flag, p.status, kStatusTimeoutSoftmax);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (__any_sync(0xffffffffu, gamma != 1.f)) {  // correction O_row *= gamma
+          {  // correction O_row *= gamma
 #pragma unroll 1
             for (int c = 0; c < kD / 32; ++c) {
               uint32_t w32[32];
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < 4; ++c4) {
           const int ch = half * 4 + c4;
-          *reinterpret_cast<uint4*>(p_row + ((ch ^ (row & 7)) << 4)) =
+          *reinterpret_cast<uint4*>(p_row0 + (j & 1) * kTile + ((ch ^ (row & 7)) << 4)) =
               make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
         }
       }
@@ -476,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack2<true>(__uint_as_float(w[2 * i]) * mul, __uint_as_float(w[2 * i + 1]) * mul);
-        uint8_t* blk = ((c / 2) ? sP : sQ) + x * kTile + row * 128;
+        uint8_t* blk = ((c / 2) ? sP + 2 * x * kTile : sQ + x * kTile) + row * 128;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int ch = (c % 2) * 4 + k;
@@ -488,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar_sync(1 + x, kBM);
       if (wq == 0 && lane == 0) {
         tma_store_3d(&tmap_o, sQ + x * kTile, 0, q0x, b * p.H + h);
-        tma_store_3d(&tmap_o, sP + x * kTile, 64, q0x, b * p.H + h);
+        tma_store_3d(&tmap_o, sP + 2 * x * kTile, 64, q0x, b * p.H + h);
         bulk_commit_group();
         bulk_wait_group_read0();
       }
