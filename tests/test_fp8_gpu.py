@@ -36,6 +36,7 @@ def _run(q, k, v, causal):
     (2, 4, 2, 257, 257, True),
     (1, 2, 2, 129, 700, False),
     (1, 2, 1, 200, 77, True),
+    (1, 2, 2, 400, 200, True),  # the first query tile of the first pair sees no key
     (1, 1, 1, 1, 1, False),
 ])
 def test_fp8_forward_vs_dequantized_oracle(shape):

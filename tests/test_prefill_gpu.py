@@ -46,6 +46,10 @@ def _run_and_compare(B, H, Hkv, Sq, Sk, d, dt, causal, seed):
     # rectangular causal, bottom-right: Sq < Sk and Sq > Sk (rows with no key)
     (1, 2, 2, 64, 1000, 128, "bf16", True),
     (1, 2, 1, 200, 77, 64, "bf16", True),
+    # Sq - Sk = 200: the first query tile of the first pair sees no key while
+    # the second does (tile L starts without waiting for tile H)
+    (1, 2, 2, 400, 200, 128, "bf16", True),
+    (1, 2, 2, 400, 200, 64, "fp16", True),
     # degenerate sizes
     (1, 1, 1, 1, 1, 64, "bf16", False),
     (1, 1, 1, 1, 1, 128, "fp16", True),
